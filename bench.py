@@ -1,0 +1,490 @@
+#!/usr/bin/env python3
+"""Benchmark: effective HBM GB/s of the low-bit QMV decode path on GB300.
+
+Workload (one "step"): the full decode sweep of a 27B-class dense layer --
+7 projections (q 6144x5120, k/v 1024x5120, o 5120x6144, gate/up 17408x5120,
+down 5120x17408) x M = 1..5 x {1-bit, 2-bit, 2-bit sym, t5} x group size
+{64, 128}: 280 QMV calls.  Each (projection, format, group size) rotates
+through 64 distinct weight sets resident in HBM (~28 GB), so every call
+streams its weights from HBM, not L2.  Effective bytes per call = packed
+weights + fp16 scales + fp16 biases (0 for sym and t5) + fp16 x + fp16 y.
+
+`value` is device-resident throughput (bytes of all calls / device time);
+`e2e` is the same through the same C-ABI calls with activations copied from
+pinned host memory and results copied back inside the timed region; the
+weights are the model's resident state.  The t5 prefill matrix product is
+timed separately (key "qmm"), in TFLOP/s.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "QMV effective HBM GB/s and % of GB300 peak, M=1-5, 1/2-bit & t5 ternary"
+UNIT = "GB/s"
+WORKLOAD = ("full decode sweep, 27B-class layer: 7 projections (q 6144x5120, k/v 1024x5120, "
+            "o 5120x6144, gate/up 17408x5120, down 5120x17408) x M 1..5 x {1-bit, 2-bit, "
+            "2-bit sym, t5} x group_size {64,128} = 280 QMV calls per step; 64 rotating "
+            "weight sets per projection/format/group size")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+F1, F2, T5 = 1, 2, 3
+VARIANTS = [("affine1", F1, False), ("affine2", F2, False), ("affine2_sym", F2, True), ("t5", T5, True)]
+GROUP_SIZES = (64, 128)
+MS = (1, 2, 3, 4, 5)
+
+
+def shapes():
+    from bit_quantized_decode_unpack_gb300.synth import LAYER_SHAPES
+    return list(LAYER_SHAPES.items())
+
+
+def call_bytes(fmt, sym, M, N, K, gs):
+    """Algorithmic bytes of one call (what the method must move)."""
+    G = K // gs
+    if fmt == F1:
+        w = N * K // 8
+    elif fmt == F2:
+        w = N * K // 4
+    else:
+        w = N * G * (-(-gs // 5))
+    has_bias = not sym and fmt != T5
+    return w + N * G * 2 + (N * G * 2 if has_bias else 0) + M * K * 2 + M * N * 2
+
+
+def page_bytes(fmt, sym, M, N, K, gs):
+    """The page's byte count (weights + scales + biases + activations)."""
+    return call_bytes(fmt, sym, M, N, K, gs) - M * N * 2
+
+
+def sweep_calls():
+    out = []
+    for M in MS:
+        for name, (N, K) in shapes():
+            for vname, fmt, sym in VARIANTS:
+                for gs in GROUP_SIZES:
+                    out.append(dict(M=M, proj=name, N=N, K=K, variant=vname, fmt=fmt, sym=sym, gs=gs))
+    return out
+
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ---- clocks -------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="bqd_clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in Path(self.path).read_text().splitlines():
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        smax = max((float(r[2]) for r in rows if r[2].replace(".", "").isdigit()), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---- our arm --------------------------------------------------------------------
+
+class Sweep:
+    """Device buffers and CUDA graphs for the decode sweep."""
+
+    def __init__(self, dev, sets: int, seed: int = 0, quick: bool = False):
+        import torch
+        import bit_quantized_decode_unpack_gb300 as bqd
+        from bit_quantized_decode_unpack_gb300 import synth
+        self.torch, self.bqd, self.dev = torch, bqd, dev
+        self.sets = sets
+        self.calls = sweep_calls()
+        if quick:
+            self.calls = [c for c in self.calls if c["proj"] in ("k_proj", "down_proj")]
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed)
+        # weight sets per (projection, group size): codes drawn and packed on the device
+        self.weights = {}
+        for name, (N, K) in shapes():
+            if quick and name not in ("k_proj", "down_proj"):
+                continue
+            for gs in GROUP_SIZES:
+                G = K // gs
+                lst = []
+                for _ in range(sets):
+                    s = synth.torch_scales(gen, N, G, dev)
+                    entry = {"scales": s,
+                             "b1": synth.torch_biases(gen, F1, s, dev),
+                             "b2": synth.torch_biases(gen, F2, s, dev)}
+                    for fmt, key in ((F1, "w1"), (F2, "w2"), (T5, "w5")):
+                        codes = synth.torch_codes(gen, fmt, N, K, dev)
+                        entry[key] = bqd.pack(codes, fmt, gs)
+                        del codes
+                    lst.append(entry)
+                self.weights[(name, gs)] = lst
+        # activations and outputs: one slab each, sliced per call
+        self.x_off, self.y_off = [], []
+        xo = yo = 0
+        for c in self.calls:
+            self.x_off.append(xo)
+            self.y_off.append(yo)
+            xo += c["M"] * c["K"] + 64  # keep 128-byte alignment between slices
+            yo += c["M"] * c["N"] + 64
+        self.x_all = synth.torch_activations(gen, 1, xo, dev).view(-1)
+        self.y_all = torch.zeros(yo, dtype=torch.float16, device=dev)
+        self.x_elems, self.y_elems = xo, yo
+        self.bytes_per_step = sum(call_bytes(c["fmt"], c["sym"], c["M"], c["N"], c["K"], c["gs"])
+                                  for c in self.calls)
+        self.page_bytes_per_step = sum(page_bytes(c["fmt"], c["sym"], c["M"], c["N"], c["K"], c["gs"])
+                                       for c in self.calls)
+        self.h2d = sum(c["M"] * c["K"] * 2 for c in self.calls)
+        self.d2h = sum(c["M"] * c["N"] * 2 for c in self.calls)
+        torch.cuda.synchronize()
+
+    def _call(self, i, c, set_idx, stream):
+        torch = self.torch
+        e = self.weights[(c["proj"], c["gs"])][set_idx]
+        M, N, K = c["M"], c["N"], c["K"]
+        x = self.x_all[self.x_off[i]:self.x_off[i] + M * K].view(M, K)
+        y = self.y_all[self.y_off[i]:self.y_off[i] + M * N].view(M, N)
+        w = {F1: e["w1"], F2: e["w2"], T5: e["w5"]}[c["fmt"]]
+        b = None
+        if not c["sym"]:
+            b = e["b1"] if c["fmt"] == F1 else e["b2"]
+        self.bqd.qmv(x, w, e["scales"], b, c["fmt"], c["gs"], out=y, stream=stream)
+
+    def capture(self, n_graphs: int):
+        """One graph per step phase; phase q uses set (5q + M - 1) mod sets."""
+        torch = self.torch
+        self.stream = torch.cuda.Stream()
+        self.graphs = []
+        with torch.cuda.stream(self.stream):
+            for q in range(n_graphs):
+                # warm (outside capture) once, then capture
+                for i, c in enumerate(self.calls):
+                    self._call(i, c, (5 * q + c["M"] - 1) % self.sets, self.stream)
+                self.stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream):
+                    for i, c in enumerate(self.calls):
+                        self._call(i, c, (5 * q + c["M"] - 1) % self.sets, self.stream)
+                self.graphs.append(g)
+        torch.cuda.synchronize()
+
+    def replay(self, step):
+        self.graphs[step % len(self.graphs)].replay()
+
+
+def time_steps(sweep, steps, warmup, e2e=False, barrier=None):
+    torch = sweep.torch
+    st = sweep.stream
+    x_host = y_host = None
+    if e2e:
+        x_host = torch.empty(sweep.x_elems, dtype=torch.float16, pin_memory=True)
+        x_host.copy_(sweep.x_all.cpu())
+        y_host = torch.empty(sweep.y_elems, dtype=torch.float16, pin_memory=True)
+
+    def one(step):
+        with torch.cuda.stream(st):
+            if e2e:
+                sweep.x_all.copy_(x_host, non_blocking=True)
+            sweep.replay(step)
+            if e2e:
+                y_host.copy_(sweep.y_all, non_blocking=True)
+
+    for w in range(warmup):
+        one(w)
+    st.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(st)
+    for s in range(steps):
+        one(warmup + s)
+    t1.record(st)
+    t1.synchronize()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return t0.elapsed_time(t1)  # ms
+
+
+def per_call_table(sweep, reps: int = 3):
+    """µs per call and effective GB/s for each (projection, variant, gs, M),
+    each timed as a graph of `sets` back-to-back calls over the rotating sets."""
+    torch = sweep.torch
+    rows = []
+    st = sweep.stream
+    for i, c in enumerate(sweep.calls):
+        with torch.cuda.stream(st):
+            for s in range(sweep.sets):
+                sweep._call(i, c, s, st)
+            st.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                for s in range(sweep.sets):
+                    sweep._call(i, c, s, st)
+        best = None
+        with torch.cuda.stream(st):
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                g.replay()
+                e1.record(st)
+                e1.synchronize()
+                t = e0.elapsed_time(e1) * 1e3 / sweep.sets
+                best = t if best is None else min(best, t)
+        nb = call_bytes(c["fmt"], c["sym"], c["M"], c["N"], c["K"], c["gs"])
+        rows.append(dict(proj=c["proj"], variant=c["variant"], gs=c["gs"], M=c["M"], us=round(best, 3),
+                         gbs=round(nb / (best * 1e-6) / 1e9, 1)))
+        del g
+    return rows
+
+
+def kernel_traffic_from_profiles():
+    """dram bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when the kernel source changed since it was taken."""
+    p = ROOT / "profiles" / "qmv_traffic.json"
+    if not p.exists():
+        return None
+    try:
+        d = json.loads(p.read_text())
+        src = ROOT / d["kernel_source"]
+        if hashlib.sha256(src.read_bytes()).hexdigest() != d["kernel_sha256"]:
+            return None
+        return d
+    except Exception:
+        return None
+
+
+# ---- CPU baseline / reference arm (the oracle on host cores) ----------------------
+
+def oracle_sample(rows_per_call: int, calls, seed=0):
+    """Time the float64 oracle on the first `rows_per_call` weight rows of each
+    call (same distributions).  Returns (bytes, seconds)."""
+    import numpy as np
+    import oracle
+    from bit_quantized_decode_unpack_gb300 import synth
+    tot_b, tot_t = 0, 0.0
+    cache = {}
+    for c in calls:
+        key = (c["proj"], c["variant"], c["gs"])
+        if key not in cache:
+            rng = np.random.default_rng(seed + len(cache))
+            R, K, gs = rows_per_call, c["K"], c["gs"]
+            codes = synth.codes(rng, c["fmt"], R, K)
+            s = synth.scales(rng, R, K // gs)
+            b = None if c["sym"] else synth.biases(rng, c["fmt"], s)
+            cache[key] = (oracle.c_pack(codes, c["fmt"], gs), s, b)
+        packed, s, b = cache[key]
+        x = synth.activations(np.random.default_rng(c["M"]), c["M"], c["K"])
+        t = time.perf_counter()
+        oracle.c_qmv_rows(x, packed, s, b, c["fmt"], c["gs"])
+        tot_t += time.perf_counter() - t
+        tot_b += call_bytes(c["fmt"], c["sym"], c["M"], rows_per_call, c["K"], c["gs"])
+    return tot_b, tot_t
+
+
+def calibrate_rows(calls, seconds: float, cap: int = 256):
+    """Rows per call so that one oracle pass over `calls` takes ~`seconds`."""
+    b, t = oracle_sample(2, calls)
+    per_row = t / 2
+    return max(1, min(cap, int(seconds / max(per_row, 1e-9)))), per_row
+
+
+def reference_arm(args):
+    """The float64 oracle as the reference arm, on host cores: every step is
+    a bounded sample of the same workload (the first R weight rows of a
+    stride-j subset of the 280 calls), sized so that the whole run ends
+    within about two minutes."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    calls = sweep_calls()
+    budget = 120.0 / max(1, args.steps + args.warmup)  # seconds per step
+    _, per_row = calibrate_rows(calls, 1.0)
+    stride = 1
+    while per_row / stride > budget and stride < len(calls):
+        stride *= 2
+    sub = calls[::stride]
+    rows = max(1, min(64, int(budget / max(per_row / stride, 1e-9))))
+    for _ in range(args.warmup):
+        oracle_sample(rows, sub)
+    b = t = 0.0
+    for _ in range(args.steps):
+        bb, tt = oracle_sample(rows, sub)
+        b += bb
+        t += tt
+    value = b / t / 1e9
+    sample = (f"first {rows} weight rows of " + ("each" if stride == 1 else f"every {stride}th") +
+              " of the 280 calls, per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- main --------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sets", type=int, default=64)
+    ap.add_argument("--quick", action="store_true", help="two projections only (development)")
+    ap.add_argument("--table", type=str, default=None, help="write the per-call table (CSV) here")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=0, help="0: sized for ~12 s of oracle work")
+    args = ap.parse_args()
+
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from bit_quantized_decode_unpack_gb300 import _build
+    _build.build()
+
+    sweep = Sweep(dev, args.sets, seed=1234 + rank, quick=args.quick)
+    n_graphs = -(-args.sets // 5) + 0
+    sweep.capture(n_graphs)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    with ClockSampler(local) as clk:
+        ms = time_steps(sweep, args.steps, args.warmup, barrier=barrier)
+    clocks = clk.summary()
+    ms_e2e = time_steps(sweep, args.steps, args.warmup, e2e=True, barrier=barrier)
+
+    def reduce_max(v):
+        if dist is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    ms, ms_e2e = reduce_max(ms), reduce_max(ms_e2e)
+    total_bytes = sweep.bytes_per_step * args.steps * world
+    value = total_bytes / (ms * 1e-3) / 1e9
+    value_e2e = total_bytes / (ms_e2e * 1e-3) / 1e9
+
+    table = None
+    if rank == 0 and args.table:
+        table = per_call_table(sweep)
+        with open(args.table, "w") as f:
+            f.write("proj,variant,gs,M,us_per_call,gbs\n")
+            for r in table:
+                f.write(f"{r['proj']},{r['variant']},{r['gs']},{r['M']},{r['us']},{r['gbs']}\n")
+
+    if rank == 0:
+        peaks, src = load_peaks()
+        hbm = float(peaks["hbm_gbs"])
+        achieved = sweep.bytes_per_step / (ms / args.steps * 1e-3) / 1e9
+        tr = kernel_traffic_from_profiles()
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "calls_per_step": len(sweep.calls),
+                       "bytes_per_step": sweep.bytes_per_step,
+                       "page_bytes_per_step": sweep.page_bytes_per_step,
+                       "weight_sets": args.sets, "l2": "inputs larger than L2 (rotating weight sets)",
+                       "accumulate": "fp32", "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "peak_source": src,
+                         "traffic": None if tr is None else tr["traffic_bytes_per_step_equiv"],
+                         "kernel": "qmv (all 280 launches of a step)",
+                         "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS},
+            "e2e": {"value": value_e2e, "unit": UNIT, "h2d_bytes_per_step": sweep.h2d,
+                    "d2h_bytes_per_step": sweep.d2h},
+            "gpu_launches": len(sweep.calls) * args.steps,
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline:
+            import oracle
+            oracle.build()
+            rows = args.cpu_rows or calibrate_rows(sweep_calls(), 12.0)[0]
+            b, t = oracle_sample(rows, sweep_calls())
+            line["cpu_baseline"] = {"value": b / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                    "sample": f"first {rows} weight rows of each of the 280 calls "
+                                              f"({t:.1f} s, one thread)"}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

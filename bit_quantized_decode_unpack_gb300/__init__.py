@@ -1,1 +1,202 @@
-"""GB300-native low-bit quantized matrix-vector product (binding placeholder)."""
+"""GB300-native low-bit quantized matrix-vector product (QMV).
+
+Thin Python binding over ``libbqd.so`` (the C ABI declared in ``include/bqd.h``).
+Every function here only marshals arguments -- torch tensors supply device
+memory and the current CUDA stream -- and calls the entry point of the same
+name; every step of the computation runs in the library's CUDA kernels.
+There is no CPU fallback: if the library is not built, calls raise.
+
+Operation (page "oMLX Bonsai 自定义内核:Qwen 系列快速 QMV 路径完整解析",
+§二.1-§二.3):  y[m, n] = sum_k x[m, k] * (scale[n, k/gs] * q[n, k] + bias[n, k/gs])
+with q packed as 1-bit / 2-bit LSB-first uint32 codes or as "t5" trits
+(five per byte, 13/26 bytes per 64/128-weight group).
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from pathlib import Path
+
+FMT_AFFINE1 = 1
+FMT_AFFINE2 = 2
+FMT_T5 = 3
+FORMATS = {"affine1": FMT_AFFINE1, "affine2": FMT_AFFINE2, "t5": FMT_T5}
+
+BQD_OK = 0
+ABI_VERSION = 1  # must match BQD_ABI_VERSION in include/bqd.h
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "_lib" / "libbqd.so"
+
+_lock = threading.Lock()
+_lib = None
+
+
+class BqdError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+def load() -> ctypes.CDLL:
+    """Load libbqd.so (built by ``_build.build()`` / ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not LIB_PATH.exists():
+            raise RuntimeError(f"{LIB_PATH} is not built: run `python -c \"import __graft_entry__ as g; "
+                               f"g.build()\"` (nvcc, sm_103a) before using the library")
+        lib = ctypes.CDLL(str(LIB_PATH))
+        i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+        lib.bqd_abi_version.argtypes = []
+        lib.bqd_abi_version.restype = i32
+        lib.bqd_status_string.argtypes = [i32]
+        lib.bqd_status_string.restype = ctypes.c_char_p
+        lib.bqd_packed_bytes.argtypes = [i32, i64, i64, i32]
+        lib.bqd_packed_bytes.restype = sz
+        lib.bqd_qmv.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, vp]
+        lib.bqd_qmv.restype = i32
+        lib.bqd_qmv_sym.argtypes = [vp, vp, vp, ctypes.c_float, i64, i64, i64, i32, i32, vp, vp]
+        lib.bqd_qmv_sym.restype = i32
+        lib.bqd_pack.argtypes = [vp, i64, i64, i32, i32, vp, vp]
+        lib.bqd_pack.restype = i32
+        lib.bqd_unpack.argtypes = [vp, i64, i64, i32, i32, vp, vp]
+        lib.bqd_unpack.restype = i32
+        lib.bqd_repack_2bit_to_t5.argtypes = [vp, i64, i64, i32, vp, vp, vp]
+        lib.bqd_repack_2bit_to_t5.restype = i32
+        lib.bqd_validate_t5.argtypes = [vp, i64, i64, i32, vp, vp]
+        lib.bqd_validate_t5.restype = i32
+        lib.bqd_detect_sym.argtypes = [vp, vp, i64, i64, ctypes.c_float, vp, vp]
+        lib.bqd_detect_sym.restype = i32
+        lib.bqd_device_status.argtypes = [vp]
+        lib.bqd_device_status.restype = i32
+        if lib.bqd_abi_version() != ABI_VERSION:
+            raise RuntimeError(f"libbqd ABI {lib.bqd_abi_version()} != binding ABI {ABI_VERSION}")
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int):
+    if status != BQD_OK:
+        raise BqdError(fn, status)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _fmt(fmt) -> int:
+    return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+# ---- host-only entry points ----------------------------------------------
+
+def abi_version() -> int:
+    return load().bqd_abi_version()
+
+
+def status_string(status: int) -> str:
+    return load().bqd_status_string(int(status)).decode()
+
+
+def packed_bytes(fmt, N: int, K: int, group_size: int) -> int:
+    return int(load().bqd_packed_bytes(_fmt(fmt), N, K, group_size))
+
+
+def row_bytes(fmt, K: int, group_size: int) -> int:
+    return packed_bytes(fmt, 1, K, group_size)
+
+
+# ---- device entry points ---------------------------------------------------
+
+def qmv(x, w_packed, scales, biases, fmt, group_size: int, out=None, stream=None):
+    """y = x @ dequant(W)^T, fp16 [M, N].  ``biases=None`` selects the sym
+    path (no bias tensor read, default ratio of the format)."""
+    import torch
+    M, K = x.shape
+    N = scales.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _check("bqd_qmv", load().bqd_qmv(_ptr(x), _ptr(w_packed), _ptr(scales), _ptr(biases), M, N, K,
+                                     _fmt(fmt), group_size, _ptr(out), _stream(stream)))
+    return out
+
+
+def qmv_sym(x, w_packed, scales, ratio: float, fmt, group_size: int, out=None, stream=None):
+    """Sym variant with an explicit ratio (bias = -ratio * scale, not read)."""
+    import torch
+    M, K = x.shape
+    N = scales.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _check("bqd_qmv_sym", load().bqd_qmv_sym(_ptr(x), _ptr(w_packed), _ptr(scales), float(ratio), M, N,
+                                             K, _fmt(fmt), group_size, _ptr(out), _stream(stream)))
+    return out
+
+
+def pack(codes, fmt, group_size: int, out=None, stream=None):
+    """codes uint8 [N, K] (device) -> packed uint8 [N, row_bytes] (device)."""
+    import torch
+    N, K = codes.shape
+    rb = row_bytes(fmt, K, group_size)
+    if out is None:
+        out = torch.empty((N, rb), dtype=torch.uint8, device=codes.device)
+    _check("bqd_pack", load().bqd_pack(_ptr(codes), N, K, _fmt(fmt), group_size, _ptr(out),
+                                       _stream(stream)))
+    return out
+
+
+def unpack(w_packed, N: int, K: int, fmt, group_size: int, out=None, stream=None):
+    import torch
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.uint8, device=w_packed.device)
+    _check("bqd_unpack", load().bqd_unpack(_ptr(w_packed), N, K, _fmt(fmt), group_size, _ptr(out),
+                                           _stream(stream)))
+    return out
+
+
+def repack_2bit_to_t5(w2, N: int, K: int, group_size: int, out=None, status=None, stream=None):
+    """-> (w_t5 uint8 [N, G*ceil(gs/5)], status int32[1] = count of codes equal to 3)."""
+    import torch
+    if out is None:
+        out = torch.empty((N, row_bytes(FMT_T5, K, group_size)), dtype=torch.uint8, device=w2.device)
+    if status is None:
+        status = torch.empty((1,), dtype=torch.int32, device=w2.device)
+    _check("bqd_repack_2bit_to_t5", load().bqd_repack_2bit_to_t5(
+        _ptr(w2), N, K, group_size, _ptr(out), _ptr(status), _stream(stream)))
+    return out, status
+
+
+def validate_t5(w_t5, N: int, K: int, group_size: int, status=None, stream=None):
+    """-> int32[1] device tensor: number of invalid t5 bytes."""
+    import torch
+    if status is None:
+        status = torch.empty((1,), dtype=torch.int32, device=w_t5.device)
+    _check("bqd_validate_t5", load().bqd_validate_t5(_ptr(w_t5), N, K, group_size, _ptr(status),
+                                                     _stream(stream)))
+    return status
+
+
+def detect_sym(scales, biases, ratio: float, out=None, stream=None):
+    """-> int32[1] device tensor: number of biases != fp16(-ratio * scale)."""
+    import torch
+    N, G = scales.shape
+    if out is None:
+        out = torch.empty((1,), dtype=torch.int32, device=scales.device)
+    _check("bqd_detect_sym", load().bqd_detect_sym(_ptr(scales), _ptr(biases), N, G, float(ratio),
+                                                   _ptr(out), _stream(stream)))
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream; BQD_OK, or the status of an expired bounded
+    device-side wait since the previous call (see include/bqd.h)."""
+    return int(load().bqd_device_status(_stream(stream)))

@@ -1,0 +1,199 @@
+// Host side of the C ABI: argument validation and dispatch by format and M
+// (the routing rules of "oMLX Bonsai 自定义内核:Qwen 系列快速 QMV 路径完整解析",
+// §二 and §三: route by bit width and by the number of activation rows).
+#include <stdlib.h>
+#include <string.h>
+
+#include "bqd_internal.cuh"
+
+namespace bqd {
+
+int sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// Testing override of the dispatcher: BQD_FORCE_KERNEL=generic|mma (read on
+// every call so that a test can compare both kernels in one process).
+static int forced_kernel()
+{
+    const char *v = getenv("BQD_FORCE_KERNEL");
+    if (v && strcmp(v, "generic") == 0) return 1;
+    if (v && strcmp(v, "mma") == 0) return 2;
+    return 0;
+}
+
+}  // namespace bqd
+
+using namespace bqd;
+
+static bool valid_format(int f) { return f == BQD_FMT_AFFINE1 || f == BQD_FMT_AFFINE2 || f == BQD_FMT_T5; }
+static bool valid_gs(int gs) { return gs == 64 || gs == 128; }
+static bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// N*K and M*K must stay far from int64 overflow; 2^50 elements is far beyond
+// any device memory.
+static bool sane(int64_t a, int64_t b) { return a >= 0 && b >= 0 && (a == 0 || b <= (int64_t(1) << 50) / a); }
+
+extern "C" int bqd_abi_version(void) { return BQD_ABI_VERSION; }
+
+extern "C" const char *bqd_status_string(int status)
+{
+    switch (status) {
+    case BQD_OK: return "ok";
+    case BQD_ERR_INVALID_ARG: return "invalid argument";
+    case BQD_ERR_UNSUPPORTED: return "unsupported request";
+    case BQD_ERR_ALIGNMENT: return "pointer alignment below the documented minimum";
+    case BQD_ERR_BAD_T5_BYTE: return "invalid t5 byte (>= 243 or non-zero padding trit)";
+    case BQD_ERR_NOT_TERNARY: return "2-bit code 3 where a ternary code was required";
+    case BQD_ERR_CUDA: return "CUDA runtime or launch error";
+    case BQD_ERR_TIMEOUT: return "bounded device-side wait expired";
+    case BQD_ERR_ABI: return "ABI version mismatch";
+    default: return "unknown status";
+    }
+}
+
+extern "C" size_t bqd_packed_bytes(int format, int64_t N, int64_t K, int group_size)
+{
+    if (!valid_format(format) || !valid_gs(group_size) || !sane(N, K) || K % group_size != 0)
+        return 0;
+    return (size_t)(N * row_bytes_of(format, K, group_size));
+}
+
+static int qmv_common(const void *x, const void *w, const void *scales, const void *biases,
+                      float ratio, int64_t M, int64_t N, int64_t K, int format, int gs,
+                      void *out, bqd_stream_t stream)
+{
+    if (!valid_format(format) || !valid_gs(gs)) return BQD_ERR_INVALID_ARG;
+    if (!sane(M, K) || !sane(N, K) || !sane(M, N) || K % gs != 0) return BQD_ERR_INVALID_ARG;
+    if (!(ratio == ratio) || ratio > 3.0e38f || ratio < -3.0e38f) return BQD_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return BQD_OK;
+    if (!out) return BQD_ERR_INVALID_ARG;
+    if (!aligned(out, 16)) return BQD_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) return cuda_status(cudaMemsetAsync(out, 0, (size_t)(M * N) * sizeof(__half), s));
+    if (!x || !w || !scales) return BQD_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(scales, 2) || (biases && !aligned(biases, 2)))
+        return BQD_ERR_ALIGNMENT;
+
+    QmvArgs a;
+    a.x = static_cast<const __half *>(x);
+    a.w = static_cast<const uint8_t *>(w);
+    a.scales = static_cast<const __half *>(scales);
+    a.biases = static_cast<const __half *>(biases);
+    a.ratio = ratio;
+    a.M = M; a.N = N; a.K = K; a.G = K / gs;
+    a.fmt = format; a.gs = gs;
+    a.row_bytes = row_bytes_of(format, K, gs);
+    a.out = static_cast<__half *>(out);
+
+    const int force = forced_kernel();
+    if (force != 1) {
+        int st = launch_qmv_mma(a, s);
+        if (st != BQD_ERR_UNSUPPORTED || force == 2) return st;
+    }
+    return launch_qmv_generic(a, s);
+}
+
+static float default_ratio(int format)
+{
+    return format == BQD_FMT_AFFINE1 ? 0.5f : (format == BQD_FMT_AFFINE2 ? 1.5f : 1.0f);
+}
+
+extern "C" int bqd_qmv(const void *x, const void *w_packed, const void *scales, const void *biases,
+                       int64_t M, int64_t N, int64_t K, int format, int group_size, void *out,
+                       bqd_stream_t stream)
+{
+    return qmv_common(x, w_packed, scales, biases, default_ratio(format), M, N, K, format,
+                      group_size, out, stream);
+}
+
+extern "C" int bqd_qmv_sym(const void *x, const void *w_packed, const void *scales, float ratio,
+                           int64_t M, int64_t N, int64_t K, int format, int group_size, void *out,
+                           bqd_stream_t stream)
+{
+    return qmv_common(x, w_packed, scales, nullptr, ratio, M, N, K, format, group_size, out, stream);
+}
+
+extern "C" int bqd_pack(const uint8_t *codes, int64_t N, int64_t K, int format, int group_size,
+                        void *w_packed, bqd_stream_t stream)
+{
+    if (!valid_format(format) || !valid_gs(group_size) || !sane(N, K) || K % group_size != 0)
+        return BQD_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return BQD_OK;
+    if (!codes || !w_packed) return BQD_ERR_INVALID_ARG;
+    if (format != BQD_FMT_T5 && !aligned(w_packed, 4)) return BQD_ERR_ALIGNMENT;
+    return launch_pack(codes, N, K, format, group_size, static_cast<uint8_t *>(w_packed),
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int bqd_unpack(const void *w_packed, int64_t N, int64_t K, int format, int group_size,
+                          uint8_t *codes, bqd_stream_t stream)
+{
+    if (!valid_format(format) || !valid_gs(group_size) || !sane(N, K) || K % group_size != 0)
+        return BQD_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return BQD_OK;
+    if (!codes || !w_packed) return BQD_ERR_INVALID_ARG;
+    if (format != BQD_FMT_T5 && !aligned(w_packed, 4)) return BQD_ERR_ALIGNMENT;
+    return launch_unpack(static_cast<const uint8_t *>(w_packed), N, K, format, group_size, codes,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int bqd_repack_2bit_to_t5(const void *w2, int64_t N, int64_t K, int group_size,
+                                     uint8_t *w_t5, int *d_status, bqd_stream_t stream)
+{
+    if (!valid_gs(group_size) || !sane(N, K) || K % group_size != 0) return BQD_ERR_INVALID_ARG;
+    if (!d_status) return BQD_ERR_INVALID_ARG;
+    if (!aligned(d_status, 4)) return BQD_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (N == 0 || K == 0) return cuda_status(cudaMemsetAsync(d_status, 0, sizeof(int), s));
+    if (!w2 || !w_t5) return BQD_ERR_INVALID_ARG;
+    if (!aligned(w2, 4)) return BQD_ERR_ALIGNMENT;
+    return launch_repack_2bit_to_t5(static_cast<const uint8_t *>(w2), N, K, group_size, w_t5,
+                                    d_status, s);
+}
+
+extern "C" int bqd_validate_t5(const uint8_t *w_t5, int64_t N, int64_t K, int group_size,
+                               int *d_status, bqd_stream_t stream)
+{
+    if (!valid_gs(group_size) || !sane(N, K) || K % group_size != 0) return BQD_ERR_INVALID_ARG;
+    if (!d_status) return BQD_ERR_INVALID_ARG;
+    if (!aligned(d_status, 4)) return BQD_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (N == 0 || K == 0) return cuda_status(cudaMemsetAsync(d_status, 0, sizeof(int), s));
+    if (!w_t5) return BQD_ERR_INVALID_ARG;
+    return launch_validate_t5(w_t5, N, K, group_size, d_status, s);
+}
+
+extern "C" int bqd_detect_sym(const void *scales, const void *biases, int64_t N, int64_t G,
+                              float ratio, int *d_mismatches, bqd_stream_t stream)
+{
+    if (!sane(N, G) || !d_mismatches) return BQD_ERR_INVALID_ARG;
+    if (!(ratio == ratio) || ratio > 3.0e38f || ratio < -3.0e38f) return BQD_ERR_INVALID_ARG;
+    if (!aligned(d_mismatches, 4)) return BQD_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (N == 0 || G == 0) return cuda_status(cudaMemsetAsync(d_mismatches, 0, sizeof(int), s));
+    if (!scales || !biases) return BQD_ERR_INVALID_ARG;
+    if (!aligned(scales, 2) || !aligned(biases, 2)) return BQD_ERR_ALIGNMENT;
+    return launch_detect_sym(static_cast<const __half *>(scales), static_cast<const __half *>(biases),
+                             N * G, ratio, d_mismatches, s);
+}
+
+extern "C" int bqd_device_status(bqd_stream_t stream)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return BQD_ERR_CUDA;
+    unsigned int n = 0;
+    const int st = take_qmv_mma_timeouts(&n);
+    if (st != BQD_OK) return st;
+    return n ? BQD_ERR_TIMEOUT : BQD_OK;
+}

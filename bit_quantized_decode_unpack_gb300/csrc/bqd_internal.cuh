@@ -1,0 +1,65 @@
+// Internal declarations shared by the libbqd translation units.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bqd.h"
+
+namespace bqd {
+
+// One QMV request after host validation.  Pointers are device pointers.
+struct QmvArgs {
+    const __half *x;       // [M, K]
+    const uint8_t *w;      // packed, row pitch = row_bytes
+    const __half *scales;  // [N, G]
+    const __half *biases;  // [N, G] or nullptr (sym)
+    float ratio;           // sym ratio, used when biases == nullptr
+    int64_t M, N, K, G, row_bytes;
+    int fmt, gs;
+    __half *out;           // [M, N]
+};
+
+inline int64_t t5_bytes_per_group(int gs) { return (gs + 4) / 5; }
+
+inline int64_t row_bytes_of(int fmt, int64_t K, int gs)
+{
+    if (fmt == BQD_FMT_AFFINE1) return K / 8;
+    if (fmt == BQD_FMT_AFFINE2) return K / 4;
+    return (K / gs) * t5_bytes_per_group(gs);
+}
+
+// Kernel launchers (return a BQD_* status).
+int launch_qmv_generic(const QmvArgs &a, cudaStream_t s);
+// Tensor-core decode path; BQD_ERR_UNSUPPORTED when the request is outside
+// its shape/alignment envelope (the caller then uses the generic kernel).
+int launch_qmv_mma(const QmvArgs &a, cudaStream_t s);
+
+int launch_pack(const uint8_t *codes, int64_t N, int64_t K, int fmt, int gs,
+                uint8_t *w, cudaStream_t s);
+int launch_unpack(const uint8_t *w, int64_t N, int64_t K, int fmt, int gs,
+                  uint8_t *codes, cudaStream_t s);
+int launch_repack_2bit_to_t5(const uint8_t *w2, int64_t N, int64_t K, int gs,
+                             uint8_t *w5, int *d_status, cudaStream_t s);
+int launch_validate_t5(const uint8_t *w5, int64_t N, int64_t K, int gs,
+                       int *d_status, cudaStream_t s);
+int launch_detect_sym(const __half *scales, const __half *biases, int64_t count,
+                      float ratio, int *d_mismatches, cudaStream_t s);
+
+// Sym bias rebuilt from a scale: fp16_rne(float(-ratio) * float(scale)).
+__device__ __forceinline__ __half sym_bias(__half s, float ratio)
+{
+    return __float2half_rn(__fmul_rn(-ratio, __half2float(s)));
+}
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? BQD_OK : BQD_ERR_CUDA; }
+
+// Reads and clears the counter of expired bounded waits of the tensor-core
+// decode kernel; BQD_OK / BQD_ERR_CUDA.
+int take_qmv_mma_timeouts(unsigned int *count);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+}  // namespace bqd

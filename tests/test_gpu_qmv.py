@@ -1,0 +1,212 @@
+"""GPU parity of the QMV path against the float64 oracle, through the C ABI.
+
+Bar: every output within |y_gpu - y| <= 2e-3 * sum_k |x_k w_k| (fp16 in,
+fp32 accumulate, fp16 out).  Small shapes span several tiles and ragged tails
+and are checked element by element on every row; the full-size shapes of the
+decode sweep are checked on sampled rows, in the same dispatch the benchmark
+times.  Both kernels (tensor-core decode and generic) are exercised.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import oracle as npo
+import bit_quantized_decode_unpack_gb300 as bqd
+from bit_quantized_decode_unpack_gb300 import synth
+from _util import assert_within_tolerance, forced_kernel, to_dev
+
+pytestmark = pytest.mark.gpu
+F1, F2, T5 = bqd.FMT_AFFINE1, bqd.FMT_AFFINE2, bqd.FMT_T5
+KERNELS = [None, "generic"]  # None = the dispatcher's choice
+
+
+def run_case(p, kernel=None, rows=None, explicit_ratio=None):
+    import torch
+    fmt, gs = p["fmt"], p["gs"]
+    packed = oracle.c_pack(p["codes"], fmt, gs)
+    w = bqd.pack(to_dev(p["codes"]), fmt, gs)
+    x, s, b = to_dev(p["x"]), to_dev(p["scales"]), to_dev(p["biases"])
+    with forced_kernel(kernel):
+        if explicit_ratio is None:
+            y = bqd.qmv(x, w, s, b, fmt, gs)
+        else:
+            y = bqd.qmv_sym(x, w, s, explicit_ratio, fmt, gs)
+    torch.cuda.synchronize()
+    yr, bound = oracle.c_qmv_rows(p["x"], packed, p["scales"], p["biases"], fmt, gs, rows=rows,
+                                  ratio=explicit_ratio)
+    yg = y.cpu().numpy().astype(np.float64)
+    if rows is not None:
+        yg = yg[:, rows]
+    return assert_within_tolerance(yg, yr, bound, what=p["key"])
+
+
+SMALL = [(1, 1, 1), (2, 17, 2), (3, 130, 5), (4, 64, 3), (5, 1000, 20), (8, 259, 32), (11, 64, 10),
+         (16, 33, 6)]  # (M, N, K in groups)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("fmt", [F1, F2, T5])
+@pytest.mark.parametrize("gs", [64, 128])
+@pytest.mark.parametrize("sym", [False, True])
+def test_small_shapes_all_rows(kernel, fmt, gs, sym):
+    for M, N, G in SMALL:
+        p = synth.problem(fmt, M, N, G * gs, gs, sym=sym)
+        if fmt == T5 and not sym:
+            # t5 with an explicit bias tensor: the general affine case
+            p["biases"] = synth.biases(np.random.default_rng(M), F2, p["scales"])
+        run_case(p, kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_config1_all_rows(kernel):
+    """1-bit, M=1, N=256, K=512, gs=64, seed 0."""
+    p = synth.problem(F1, 1, 256, 512, 64, key="affine1_m1_256x512_gs64")
+    run_case(p, kernel)
+
+
+def _sample_rows(N, n=48, seed=0):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, 1, 15, 16, N - 1], rng.integers(0, N, n)]))
+
+
+FULL = []
+for (N, K) in [(5120, 5120), (1024, 5120), (17408, 5120), (5120, 17408)]:
+    for gs in (64, 128):
+        for M in (1, 5):
+            FULL.append((F2, M, N, K, gs, False))
+    FULL.append((F2, 3, N, K, 64, True))
+for (N, K) in [(17408, 5120), (5120, 17408)]:
+    for gs in (64, 128):
+        for M in (1, 3, 5):
+            FULL.append((T5, M, N, K, gs, True))
+for (N, K) in [(6144, 5120), (5120, 6144), (17408, 5120)]:
+    FULL.append((F1, 1, N, K, 64, False))
+    FULL.append((F1, 5, N, K, 128, False))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("fmt,M,N,K,gs,sym", FULL)
+def test_full_size_sampled_rows(fmt, M, N, K, gs, sym):
+    p = synth.problem(fmt, M, N, K, gs, sym=sym)
+    run_case(p, None, rows=_sample_rows(N, seed=N + K + M))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("fmt,ratio", [(F1, 0.5), (F2, 1.5), (T5, 1.0)])
+def test_sym_identity_on_gpu_is_bit_identical(kernel, fmt, ratio):
+    """§二.2 identity I-B: the bias-free path equals the path reading the
+    stored bias fp16(-ratio*scale), bit for bit."""
+    import torch
+    p = synth.problem(fmt, 5, 777, 1280, 64, sym=True)
+    stored = npo.sym_bias(p["scales"], ratio)
+    w = bqd.pack(to_dev(p["codes"]), fmt, 64)
+    x, s = to_dev(p["x"]), to_dev(p["scales"])
+    with forced_kernel(kernel):
+        y0 = bqd.qmv(x, w, s, None, fmt, 64)
+        y1 = bqd.qmv(x, w, s, to_dev(stored), fmt, 64)
+        y2 = bqd.qmv_sym(x, w, s, ratio, fmt, 64)
+    torch.cuda.synchronize()
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    assert torch.equal(y0.view(torch.int16), y2.view(torch.int16))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_explicit_ratio(kernel):
+    p = synth.problem(F2, 4, 300, 1024, 128, sym=True)
+    run_case(p, kernel, explicit_ratio=0.7)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_kernels_agree_and_are_deterministic(kernel):
+    import torch
+    p = synth.problem(F2, 5, 2048, 5120, 64)
+    w = bqd.pack(to_dev(p["codes"]), F2, 64)
+    x, s, b = to_dev(p["x"]), to_dev(p["scales"]), to_dev(p["biases"])
+    with forced_kernel(kernel):
+        y0 = bqd.qmv(x, w, s, b, F2, 64)
+        y1 = bqd.qmv(x, w, s, b, F2, 64)
+    torch.cuda.synchronize()
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+
+
+def test_empty_and_degenerate_inputs():
+    import torch
+    dev = "cuda"
+    poison = torch.full((4, 8), 7.0, dtype=torch.float16, device=dev)
+    x = torch.zeros((4, 64), dtype=torch.float16, device=dev)
+    s = torch.ones((8, 1), dtype=torch.float16, device=dev)
+    w = torch.zeros((8, 16), dtype=torch.uint8, device=dev)
+    # M = 0 / N = 0: valid no-ops
+    bqd.qmv(x[:0], w, s, None, F2, 64, out=poison[:0])
+    lib = bqd.load()
+    assert lib.bqd_qmv(None, None, None, None, 4, 0, 64, F2, 64, None, None) == 0
+    torch.cuda.synchronize()
+    assert torch.all(poison == 7.0)
+    # K = 0: zeros
+    out = torch.full((4, 8), 7.0, dtype=torch.float16, device=dev)
+    assert lib.bqd_qmv(None, None, None, None, 4, 8, 0, F2, 64,
+                       __import__("ctypes").c_void_p(out.data_ptr()), None) == 0
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)
+    # x = 0: exact zeros for every format (bias times a zero sum)
+    for fmt in (F1, F2, T5):
+        p = synth.problem(fmt, 3, 70, 640, 64)
+        wd = bqd.pack(to_dev(p["codes"]), fmt, 64)
+        for kernel in KERNELS:
+            with forced_kernel(kernel):
+                y = bqd.qmv(torch.zeros((3, 640), dtype=torch.float16, device=dev), wd,
+                            to_dev(p["scales"]), to_dev(p["biases"]), fmt, 64)
+            torch.cuda.synchronize()
+            assert torch.all(y == 0)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("fmt", [F1, F2, T5])
+def test_one_hot_x_recovers_dequantized_weights(kernel, fmt):
+    import torch
+    gs, N, K = 64, 96, 256
+    p = synth.problem(fmt, 8, N, K, gs)
+    ks = [0, 1, 63, 64, 130, 255, 200, 17]
+    x = np.zeros((8, K), dtype=np.float16)
+    for m, k in enumerate(ks):
+        x[m, k] = 1
+    p["x"] = x
+    run_case(p, kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_output_guard_band_untouched(kernel):
+    import torch
+    p = synth.problem(F2, 5, 1000, 1280, 64)
+    w = bqd.pack(to_dev(p["codes"]), F2, 64)
+    M, N = 5, 1000
+    buf = torch.full((M * N + 2048,), 1234.0, dtype=torch.float16, device="cuda")
+    out = buf[:M * N].view(M, N)
+    with forced_kernel(kernel):
+        bqd.qmv(to_dev(p["x"]), w, to_dev(p["scales"]), to_dev(p["biases"]), F2, 64, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(buf[M * N:] == 1234.0)
+
+
+def test_large_magnitudes_stay_within_tolerance():
+    """Scales near 8, x up to +-60: fp16 output stays finite and within bound."""
+    rng = np.random.default_rng(9)
+    p = synth.problem(F2, 3, 200, 640, 64)
+    p["scales"] = (np.abs(rng.normal(0, 2, size=p["scales"].shape)) + 6).astype(np.float16)
+    p["biases"] = (-p["scales"].astype(np.float32) * 1.5).astype(np.float16)
+    p["x"] = (rng.normal(0, 20, size=p["x"].shape)).clip(-60, 60).astype(np.float16) * np.float16(0.01)
+    for kernel in KERNELS:
+        run_case(p, kernel)
+
+
+def test_non_default_stream():
+    import torch
+    p = synth.problem(T5, 5, 500, 1280, 128, sym=True)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        w = bqd.pack(to_dev(p["codes"]), T5, 128)
+        y = bqd.qmv(to_dev(p["x"]), w, to_dev(p["scales"]), None, T5, 128)
+    st.synchronize()
+    packed = oracle.c_pack(p["codes"], T5, 128)
+    yr, bound = oracle.c_qmv_rows(p["x"], packed, p["scales"], None, T5, 128)
+    assert_within_tolerance(y.cpu().numpy(), yr, bound)
