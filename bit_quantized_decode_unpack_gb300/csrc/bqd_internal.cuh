@@ -35,6 +35,8 @@ int launch_qmv_generic(const QmvArgs &a, cudaStream_t s);
 // Tensor-core decode path; BQD_ERR_UNSUPPORTED when the request is outside
 // its shape/alignment envelope (the caller then uses the generic kernel).
 int launch_qmv_mma(const QmvArgs &a, cudaStream_t s);
+// Tensor-core decode path for t5 weights (K a multiple of 1024); same contract.
+int launch_qmv_t5(const QmvArgs &a, cudaStream_t s);
 
 int launch_pack(const uint8_t *codes, int64_t N, int64_t K, int fmt, int gs,
                 uint8_t *w, cudaStream_t s);
@@ -58,6 +60,7 @@ inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? BQD_OK : BQD_E
 // Reads and clears the counter of expired bounded waits of the tensor-core
 // decode kernel; BQD_OK / BQD_ERR_CUDA.
 int take_qmv_mma_timeouts(unsigned int *count);
+int take_qmv_t5_timeouts(unsigned int *count);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

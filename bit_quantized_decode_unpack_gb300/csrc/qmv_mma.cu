@@ -31,11 +31,25 @@
 #include <mutex>
 
 #include "bqd_internal.cuh"
+#include "qmv_common.cuh"
 
 namespace bqd {
 namespace {
 
-constexpr int kWarps = 8;
+using namespace qmvdev;
+
+// Number of bounded device-side waits that expired (read by bqd_device_status).
+__device__ unsigned int g_qmv_mma_timeouts = 0;
+
+// Bounded wait: false (and the timeout counter bumped) if the phase never completes.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < kWaitSpins; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    atomicAdd(&g_qmv_mma_timeouts, 1u);
+    return false;
+}
+
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxM = 8;
 constexpr int kMaxTc = 8;
@@ -55,134 +69,6 @@ struct Params {
     long long row_bytes;
     int tiles, chunks, S, Tc, Cs;
 };
-
-// ---- PTX helpers -------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b)
-{
-    uint32_t d;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
-{
-    uint32_t d;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-// (a & MASK) | c in one LOP3, MASK an immediate, c a register
-template <uint32_t MASK>
-__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c)
-{
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
-    return d;
-}
-
-__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void mma1688(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(b0));
-}
-
-
-
-
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void st_cluster_f32(uint32_t local_addr, uint32_t rank, float v)
-{
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
-}
-
-// Number of bounded device-side waits that expired (read by bqd_device_status).
-__device__ unsigned int g_qmv_mma_timeouts = 0;
-constexpr uint32_t kWaitSpins = 1u << 22;  // ~ a second of try_wait round trips
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait: false (and the timeout counter bumped) if the phase never completes.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
-{
-    for (uint32_t i = 0; i < kWaitSpins; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    atomicAdd(&g_qmv_mma_timeouts, 1u);
-    return false;
-}
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
-
-__device__ __forceinline__ uint32_t dup_half(uint16_t h) { return (uint32_t)h | ((uint32_t)h << 16); }
-
-// fp16 bits of a value 2^(10-p) + q whose code field q sits at mantissa bit p
-__host__ __device__ constexpr uint32_t magic(int p) { return (uint32_t)((25 - p) << 10) * 0x00010001u; }
 
 // ---- format traits -----------------------------------------------------------
 
@@ -277,88 +163,6 @@ struct UnitData {
     uint4 w0, w1;     // slice of row g / row g+8 (1-bit uses .x, .y)
     uint16_t s0, s1;  // scale of the slice's group, rows g / g+8
     uint16_t b0, b1;  // bias (sym: scale) of the bias-MMA group, rows g / g+8
-};
-
-__device__ __forceinline__ uint4 ld_stream_v4(const void *p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ uint2 ld_stream_v2(const void *p)
-{
-    uint2 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ uint16_t ld_u16(const __half *p)
-{
-    uint16_t v;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ uint4 ld_stream_v4_if(const void *p, bool pred)
-{
-    uint4 v;
-    asm volatile(
-        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
-        "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
-        "@q ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n\t}"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p), "r"((int)pred));
-    return v;
-}
-
-__device__ __forceinline__ uint2 ld_stream_v2_if(const void *p, bool pred)
-{
-    uint2 v;
-    asm volatile(
-        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %3, 0;\n\tmov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\t"
-        "@q ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];\n\t}"
-        : "=r"(v.x), "=r"(v.y)
-        : "l"(p), "r"((int)pred));
-    return v;
-}
-
-__device__ __forceinline__ uint16_t ld_u16_if(const __half *p, bool pred)
-{
-    uint16_t v;
-    asm volatile(
-        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\tmov.b16 %0, 0;\n\t@q ld.global.nc.u16 %0, [%1];\n\t}"
-        : "=h"(v)
-        : "l"(p), "r"((int)pred));
-    return v;
-}
-
-// Position of one warp in its unit sequence u = warp, warp+8, ... (tile-major;
-// a unit is 16 weight rows x one 256-code chunk).
-struct UnitPos {
-    int tl, cl;
-    __device__ __forceinline__ void start(int warp, int ncl)
-    {
-        tl = 0;
-        cl = warp;
-        while (cl >= ncl) {
-            cl -= ncl;
-            ++tl;
-        }
-    }
-    // returns the number of row tiles crossed
-    __device__ __forceinline__ int advance(int ncl)
-    {
-        int crossed = 0;
-        cl += kWarps;
-        while (cl >= ncl) {
-            cl -= ncl;
-            ++crossed;
-        }
-        tl += crossed;
-        return crossed;
-    }
 };
 
 // Global addresses of one warp's next unit to load, advanced incrementally.

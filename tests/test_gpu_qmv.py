@@ -17,7 +17,7 @@ from _util import assert_within_tolerance, forced_kernel, to_dev
 
 pytestmark = pytest.mark.gpu
 F1, F2, T5 = bqd.FMT_AFFINE1, bqd.FMT_AFFINE2, bqd.FMT_T5
-KERNELS = [None, "generic"]  # None = the dispatcher's choice
+KERNELS = [None, "generic"]  # None = the dispatcher's choice; "mma" forces the tensor-core paths
 
 
 def run_case(p, kernel=None, rows=None, explicit_ratio=None):
@@ -57,6 +57,25 @@ def test_small_shapes_all_rows(kernel, fmt, gs, sym):
         run_case(p, kernel)
 
 
+# shapes inside the tensor-core paths' envelope (t5: K a multiple of 1024),
+# spanning several row tiles, K-slices and ragged row tails
+MMA_SHAPES = [(1, 17, 1024), (2, 300, 2048), (3, 130, 3072), (5, 1000, 1024), (8, 259, 2048), (11, 40, 1024),
+              (4, 16, 5120), (6, 1, 1024)]
+
+
+@pytest.mark.parametrize("fmt", [F1, F2, T5])
+@pytest.mark.parametrize("gs", [64, 128])
+@pytest.mark.parametrize("sym", [False, True])
+def test_tensor_core_paths_forced(fmt, gs, sym):
+    """BQD_FORCE_KERNEL=mma makes an unsupported request an error instead of
+    a fallback, so these cases are known to run on the tensor-core kernels."""
+    for M, N, K in MMA_SHAPES:
+        p = synth.problem(fmt, M, N, K, gs, sym=sym)
+        if fmt == T5 and not sym:
+            p["biases"] = synth.biases(np.random.default_rng(N), F2, p["scales"])
+        run_case(p, "mma")
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_config1_all_rows(kernel):
     """1-bit, M=1, N=256, K=512, gs=64, seed 0."""
@@ -91,13 +110,13 @@ def test_full_size_sampled_rows(fmt, M, N, K, gs, sym):
     run_case(p, None, rows=_sample_rows(N, seed=N + K + M))
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kernel", KERNELS + ["mma"])
 @pytest.mark.parametrize("fmt,ratio", [(F1, 0.5), (F2, 1.5), (T5, 1.0)])
 def test_sym_identity_on_gpu_is_bit_identical(kernel, fmt, ratio):
     """§二.2 identity I-B: the bias-free path equals the path reading the
     stored bias fp16(-ratio*scale), bit for bit."""
     import torch
-    p = synth.problem(fmt, 5, 777, 1280, 64, sym=True)
+    p = synth.problem(fmt, 5, 777, 2048, 64, sym=True)
     stored = npo.sym_bias(p["scales"], ratio)
     w = bqd.pack(to_dev(p["codes"]), fmt, 64)
     x, s = to_dev(p["x"]), to_dev(p["scales"])
@@ -116,7 +135,7 @@ def test_explicit_ratio(kernel):
     run_case(p, kernel, explicit_ratio=0.7)
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kernel", KERNELS + ["mma"])
 def test_kernels_agree_and_are_deterministic(kernel):
     import torch
     p = synth.problem(F2, 5, 2048, 5120, 64)
@@ -186,6 +205,18 @@ def test_output_guard_band_untouched(kernel):
         bqd.qmv(to_dev(p["x"]), w, to_dev(p["scales"]), to_dev(p["biases"]), F2, 64, out=out)
     torch.cuda.synchronize()
     assert torch.all(buf[M * N:] == 1234.0)
+
+
+@pytest.mark.parametrize("fmt", [F1, F2, T5])
+def test_large_scales_take_the_exact_unpack(fmt):
+    """Scales far above the fast unpack's range (|s| up to ~600) must still be
+    exact on the tensor-core paths (they switch to the exact unpack)."""
+    rng = np.random.default_rng(4)
+    p = synth.problem(fmt, 2, 96, 2048, 64, sym=True)
+    p["scales"] = (np.abs(rng.normal(0, 200, size=p["scales"].shape)) + 1).astype(np.float16)
+    p["x"] = (p["x"].astype(np.float32) * 1e-3).astype(np.float16)
+    run_case(p, "mma")
+    run_case(p, None)
 
 
 def test_large_magnitudes_stay_within_tolerance():
