@@ -137,6 +137,23 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+# ---- replicas: timing aggregation over ranks ----------------------------------------
+
+def max_over_ranks(v: float, dist=None, device=None) -> float:
+    """The step time every rank reports: the slowest rank's."""
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step_per_rank: int, steps: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput: bytes moved by all replicas over the slowest rank's time."""
+    return bytes_per_step_per_rank * steps * world / (ms_max * 1e-3) / 1e9
+
+
 # ---- our arm --------------------------------------------------------------------
 
 class Sweep:
@@ -294,19 +311,57 @@ def per_call_table(sweep, reps: int = 3):
 
 
 def kernel_traffic_from_profiles():
-    """dram bytes per launch of the dominant kernel from the committed ncu
-    summary, or None when the kernel source changed since it was taken."""
+    """DRAM-bytes / algorithmic-bytes ratio of the QMV kernels from the committed
+    ncu summaries, or None when a kernel source changed since it was taken."""
     p = ROOT / "profiles" / "qmv_traffic.json"
     if not p.exists():
         return None
     try:
         d = json.loads(p.read_text())
-        src = ROOT / d["kernel_source"]
-        if hashlib.sha256(src.read_bytes()).hexdigest() != d["kernel_sha256"]:
-            return None
-        return d
+        for src, digest in d["kernel_sha256"].items():
+            if hashlib.sha256((ROOT / src).read_bytes()).hexdigest() != digest:
+                return None
+        ratios = list(d["dram_over_algorithmic"].values())
+        return sum(ratios) / len(ratios)
     except Exception:
         return None
+
+
+def run_case(spec: str, sets: int, reps: int = 64):
+    """--case fmt,M,N,K,gs[,sym]: one configuration over rotating weight sets
+    (the driver used for single-kernel ncu captures)."""
+    import torch
+    import bit_quantized_decode_unpack_gb300 as bqd
+    from bit_quantized_decode_unpack_gb300 import _build, synth
+    _build.build()
+    f = spec.split(",")
+    fmt, M, N, K, gs = (int(v) for v in f[:5])
+    sym = len(f) > 5 and f[5] == "sym"
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    W = []
+    for _ in range(sets):
+        s_ = synth.torch_scales(gen, N, K // gs, dev)
+        b_ = None if sym else synth.torch_biases(gen, fmt, s_, dev)
+        W.append((bqd.pack(synth.torch_codes(gen, fmt, N, K, dev), fmt, gs), s_, b_))
+    x = synth.torch_activations(gen, M, K, dev)
+    y = torch.empty(M, N, dtype=torch.float16, device=dev)
+    for i in range(4):
+        w, s_, b_ = W[i % sets]
+        bqd.qmv(x, w, s_, b_, fmt, gs, out=y)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(reps):
+        w, s_, b_ = W[i % sets]
+        bqd.qmv(x, w, s_, b_, fmt, gs, out=y)
+    e1.record()
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    nb = call_bytes(fmt, sym or fmt == T5, M, N, K, gs)
+    print(json.dumps({"case": spec, "us_per_call_eager": us, "gbs": nb / (us * 1e-6) / 1e9}), flush=True)
+    return 0
 
 
 # ---- CPU baseline / reference arm (the oracle on host cores) ----------------------
@@ -395,7 +450,11 @@ def main():
     ap.add_argument("--table", type=str, default=None, help="write the per-call table (CSV) here")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=0, help="0: sized for ~12 s of oracle work")
+    ap.add_argument("--case", type=str, default=None, help="fmt,M,N,K,gs[,sym]: time one configuration")
     args = ap.parse_args()
+
+    if args.case:
+        return run_case(args.case, args.sets)
 
     if args.impl == "reference":
         return reference_arm(args)
@@ -427,17 +486,10 @@ def main():
     clocks = clk.summary()
     ms_e2e = time_steps(sweep, args.steps, args.warmup, e2e=True, barrier=barrier)
 
-    def reduce_max(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    ms, ms_e2e = reduce_max(ms), reduce_max(ms_e2e)
-    total_bytes = sweep.bytes_per_step * args.steps * world
-    value = total_bytes / (ms * 1e-3) / 1e9
-    value_e2e = total_bytes / (ms_e2e * 1e-3) / 1e9
+    ms = max_over_ranks(ms, dist, dev)
+    ms_e2e = max_over_ranks(ms_e2e, dist, dev)
+    value = whole_job_gbs(sweep.bytes_per_step, args.steps, world, ms)
+    value_e2e = whole_job_gbs(sweep.bytes_per_step, args.steps, world, ms_e2e)
 
     table = None
     if rank == 0 and args.table:
@@ -463,7 +515,9 @@ def main():
                        "accumulate": "fp32", "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_source": src,
-                         "traffic": None if tr is None else tr["traffic_bytes_per_step_equiv"],
+                         "traffic": None if tr is None else tr * sweep.bytes_per_step,
+                         "traffic_basis": "dram bytes / algorithmic bytes of single-launch ncu captures "
+                                          "(profiles/qmv_traffic.json) x bytes per step",
                          "kernel": "qmv (all 280 launches of a step)",
                          "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS},
             "e2e": {"value": value_e2e, "unit": UNIT, "h2d_bytes_per_step": sweep.h2d,

@@ -179,6 +179,16 @@ __device__ __forceinline__ uint2 ld_stream_v2_if(const void *p, bool pred)
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_u32_if(const void *p, bool pred)
+{
+    uint32_t v;
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\tmov.b32 %0, 0;\n\t@q ld.global.nc.u32 %0, [%1];\n\t}"
+        : "=r"(v)
+        : "l"(p), "r"((int)pred));
+    return v;
+}
+
 __device__ __forceinline__ uint16_t ld_u16_if(const __half *p, bool pred)
 {
     uint16_t v;

@@ -28,6 +28,9 @@
 // loads, two units ahead; the first units are requested before the
 // programmatic-dependent-launch wait (weights never depend on the previous
 // kernel).
+#include <stdio.h>
+#include <stdlib.h>
+
 #include <mutex>
 
 #include "bqd_internal.cuh"
@@ -672,6 +675,9 @@ int launch_qmv_mma(const QmvArgs &a, cudaStream_t s)
         p.x = a.x + m0 * a.K;
         p.out = a.out + m0 * a.N;
         p.S = pl.S; p.Tc = pl.Tc; p.Cs = pl.Cs;
+        if (getenv("BQD_DEBUG_PLAN"))
+            fprintf(stderr, "bqd %s plan: N=%d K=%d M=%d gs=%d -> S=%d Tc=%d Cs=%d R=%d grid=%d smem=%zu\n", "mma",
+                    p.N, p.K, M, a.gs, pl.S, pl.Tc, pl.Cs, pl.R, pl.R * pl.S, pl.smem);
         const int st = a.fmt == BQD_FMT_AFFINE2 ? launch_fmt<BQD_FMT_AFFINE2>(p, pl, a.biases != nullptr, s)
                                                 : launch_fmt<BQD_FMT_AFFINE1>(p, pl, a.biases != nullptr, s);
         if (st != BQD_OK) return st;

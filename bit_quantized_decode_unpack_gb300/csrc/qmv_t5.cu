@@ -23,7 +23,11 @@
 // trit one LOP3 (mask + magic exponent) and one HFMA2 (s*t with per-half
 // scales).  A group's last byte carries padding trits (0), whose B entries
 // are 0.
+#include <stdio.h>
+#include <stdlib.h>
+
 #include <mutex>
+#include <type_traits>
 
 #include "bqd_internal.cuh"
 #include "qmv_common.cuh"
@@ -35,14 +39,13 @@ using namespace qmvdev;
 
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxM = 8;
-constexpr int kMaxTc = 4;
+constexpr int kMaxTc = 8;
 constexpr int kChunkBytes = 208;  // per weight row and unit
 constexpr int kChunkCodes = 1024;
 constexpr int kSliceWords = 13;   // 52 bytes per thread
 constexpr int kMmas = 65;         // per unit: 26 byte pairs x 5 trits x 2 halves / 8 per MMA row
-constexpr int kStages = 2;
+constexpr int kMaxStages = 2;
 constexpr int kStageBytes = 16 * kChunkBytes;
-constexpr int kStageArea = kWarps * kStages * kStageBytes;
 constexpr size_t kSmemBudget = 112 * 1024;
 
 __device__ unsigned int g_qmv_t5_timeouts = 0;
@@ -64,7 +67,7 @@ struct T5Params {
     float ratio;
     int M, N, K, G;
     long long row_bytes;
-    int tiles, chunks, S, Tc, Cs;
+    int tiles, chunks, S, Tc, Cs, NS;  // NS: stages per warp (1 or 2)
     uint32_t zero;  // always 0: keeps the magic constants in registers
 };
 
@@ -92,7 +95,7 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_t5_kernel(const T5Params p)
     using Ge = Geo<GS>;
     constexpr int B = Ge::B;
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ __align__(8) uint64_t fullbar[kWarps][kStages];
+    __shared__ __align__(8) uint64_t fullbar[kWarps][kMaxStages];
     __shared__ __align__(8) uint64_t xbar;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -104,16 +107,19 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_t5_kernel(const T5Params p)
     const int ncl = max(0, min(p.Cs, p.chunks - c_lo));
     const int M = p.M;
 
-    // shared memory: [lut][stages | raw x][Bs][SxB][accW][accC]
+    // shared memory: [lut][stages][Bs][SxB][raw x | accW accC]
+    const int NS = p.NS;
     uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
     uint8_t *stages = smem + 1024;
-    __half *xr = reinterpret_cast<__half *>(stages);  // prologue only: [M][Cs*1024]
-    uint2 *Bs = reinterpret_cast<uint2 *>(stages + kStageArea);            // [Cs][65][M][4] (+32 pad)
-    uint2 *SxB = Bs + (size_t)p.Cs * kMmas * M * 4 + 32;                   // [Cs][NB][M][4] (+32 pad)
-    float *accW = reinterpret_cast<float *>(SxB + (size_t)p.Cs * Ge::NB * M * 4 + 32);  // [warps][Tc][128]
-    float *accC = accW + (size_t)kWarps * p.Tc * 128;                      // [S][Tc][128]
+    // B fragments [Cs][M][4 slots][65 MMAs] (MMA index innermost: one base per
+    // unit, immediate offsets per MMA)
+    uint2 *Bs = reinterpret_cast<uint2 *>(stages + (size_t)kWarps * NS * kStageBytes);
+    uint2 *SxB = Bs + (size_t)p.Cs * M * 4 * kMmas + 8 * 4 * kMmas;        // [Cs][NB][M][4] (+32 pad)
+    uint8_t *region = reinterpret_cast<uint8_t *>(SxB + (size_t)p.Cs * Ge::NB * M * 4 + 32);
+    __half *xr = reinterpret_cast<__half *>(region);                       // prologue only: [M][Cs*1024]
+    float *accW = reinterpret_cast<float *>(region);                      // [warps][Tc][16][M]
+    float *accC = accW + (size_t)kWarps * p.Tc * 16 * M;                   // [S][Tc][16][M]
     const int xs = p.Cs * kChunkCodes;  // raw x row stride (halves)
-
     // decode table: byte -> five trits at bits 0,2,4,6,8 (invalid bytes -> 0)
     {
         int v = tid, e = 0;
@@ -128,10 +134,8 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_t5_kernel(const T5Params p)
     }
     const uint32_t xb = smem_addr(&xbar);
     if (tid == 0) mbar_init(xb, 1);
-    if (lane == 0) {
-        mbar_init(smem_addr(&fullbar[warp][0]), 1);
-        mbar_init(smem_addr(&fullbar[warp][1]), 1);
-    }
+    if (lane == 0)
+        for (int st = 0; st < NS; ++st) mbar_init(smem_addr(&fullbar[warp][st]), 1);
 
     pdl_wait();
     __syncthreads();
@@ -150,30 +154,30 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_t5_kernel(const T5Params p)
     if (!alive && tid == 0 && slice_codes > 0) mbar_wait_bounded(xb, 0);
 
     if (alive) {
-        // B fragments: entry (cl, i, m, tt) = R0 (half2 2i), R1 (half2 2i+1) of slot tt
-        const int entries = ncl * kMmas * M * 4;
-        for (int e = tid; e < entries; e += kThreads) {
-            const int tt = e & 3, m = (e >> 2) % M, i = (e / (4 * M)) % kMmas, cl = e / (4 * M * kMmas);
-            uint32_t r[2];
+        // B fragments: entry (cl, i, m, tt) = R0 (half2 2i), R1 (half2 2i+1) of
+        // slot tt.  A thread owns fixed (i, tt) -- its four chunk-local code
+        // offsets need only compile-time divisors -- and walks (cl, m).
+        for (int it = tid; it < kMmas * 4; it += kThreads) {
+            const int i = it >> 2, tt = it & 3;
+            int kc[4];  // (slot, half) -> code within the chunk, -1 for a padding trit
 #pragma unroll
-            for (int sl = 0; sl < 2; ++sl) {
+            for (int q = 0; q < 4; ++q) {
+                const int sl = q >> 1, hi = q & 1;
                 const int h = 2 * i + sl, j = h / 5, d = h % 5;
-                uint32_t packed = 0;
-#pragma unroll
-                for (int hi = 0; hi < 2; ++hi) {
-                    const int o = Ge::byte_a(j) + hi * B;     // byte within the 52-byte slice
-                    const int q = o / B, bg = o % B;           // slice-local group, byte in group
-                    const int within = 5 * bg + d;
-                    uint16_t bits = 0;
-                    if (within < GS) {
-                        const int kc = (Ge::NG * tt + q) * GS + within;  // code within the chunk
-                        bits = __half_as_ushort(xr[(size_t)m * xs + cl * kChunkCodes + kc]);
-                    }
-                    packed |= (uint32_t)bits << (16 * hi);
-                }
-                r[sl] = packed;
+                const int o = Ge::byte_a(j) + hi * B;  // byte within the 52-byte slice
+                const int grp = o / B, bg = o % B;      // slice-local group, byte in group
+                const int within = 5 * bg + d;
+                kc[q] = within < GS ? (Ge::NG * tt + grp) * GS + within : -1;
             }
-            Bs[e] = make_uint2(r[0], r[1]);
+            for (int cl = 0; cl < ncl; ++cl) {
+                for (int m = 0; m < M; ++m) {
+                    const uint16_t *src = reinterpret_cast<const uint16_t *>(xr) + (size_t)m * xs + cl * kChunkCodes;
+                    uint32_t v[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) v[q] = kc[q] >= 0 ? src[kc[q]] : 0u;
+                    Bs[((size_t)(cl * M + m) * 4 + tt) * kMmas + i] = make_uint2(v[0] | (v[1] << 16), v[2] | (v[3] << 16));
+                }
+            }
         }
         // bias MMA operands: groups gA = NG*tt + 2*nb, gB = gA + 1, (Sx_hi, Sx_lo) each
         const int sentries = ncl * Ge::NB * M * 4;
@@ -197,23 +201,29 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_t5_kernel(const T5Params p)
             SxB[e] = make_uint2(r[0], r[1]);
         }
     }
-    for (int e = tid; e < kWarps * p.Tc * 128; e += kThreads) accW[e] = 0.f;
-    __syncthreads();  // raw x consumed: the stage ring may now be filled
+    __syncthreads();  // raw x consumed: its space becomes the accumulators
+    for (int e = tid; e < kWarps * p.Tc * 16 * M; e += kThreads) accW[e] = 0.f;
+    __syncthreads();
     if (S > 1) cluster_sync();
     pdl_launch_dependents();
 
     // ---- per-warp stage ring --------------------------------------------------
-    uint8_t *my_stages = stages + (size_t)warp * kStages * kStageBytes;
+    uint8_t *my_stages = stages + (size_t)warp * NS * kStageBytes;
+    // one 208-byte bulk copy per weight row, issued by lanes 0..15
     auto issue = [&](int nidx, const UnitPos &pos) {
-        if (lane != 0 || pos.tl >= ntile) return;
+        if (pos.tl >= ntile) return;
         const int rowbase = (tile0 + pos.tl) * 16;
         const int nvalid = min(16, p.N - rowbase);
-        const uint32_t bar = smem_addr(&fullbar[warp][nidx & 1]);
-        const uint32_t dst = smem_addr(my_stages + (nidx & 1) * kStageBytes);
-        mbar_arrive_expect_tx(bar, (uint32_t)(nvalid * kChunkBytes));
-        const uint8_t *src = p.w + (long long)rowbase * p.row_bytes + (long long)(c_lo + pos.cl) * kChunkBytes;
-        for (int r = 0; r < nvalid; ++r)
-            bulk_g2s(dst + r * kChunkBytes, src + (long long)r * p.row_bytes, kChunkBytes, bar);
+        const int st = NS == 2 ? (nidx & 1) : 0;
+        const uint32_t bar = smem_addr(&fullbar[warp][st]);
+        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nvalid * kChunkBytes));
+        __syncwarp();
+        if (lane < nvalid) {
+            const uint32_t dst = smem_addr(my_stages + st * kStageBytes + lane * kChunkBytes);
+            const uint8_t *src = p.w + (long long)(rowbase + lane) * p.row_bytes +
+                                 (long long)(c_lo + pos.cl) * kChunkBytes;
+            bulk_g2s(dst, src, kChunkBytes, bar);
+        }
     };
 
     uint32_t mg[5];
@@ -223,31 +233,45 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_t5_kernel(const T5Params p)
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
     auto flush = [&](int tl) {
-        float *dst = accW + ((size_t)warp * p.Tc + tl) * 128;
+        float *dst = accW + ((size_t)warp * p.Tc + tl) * 16 * M;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            dst[(g + 8 * (q >> 1)) * 8 + 2 * t + (q & 1)] = (acc[0][q] + acc[1][q]) + (acc[2][q] + acc[3][q]);
+            const int col = 2 * t + (q & 1);
+            if (col < M) dst[(g + 8 * (q >> 1)) * M + col] = (acc[0][q] + acc[1][q]) + (acc[2][q] + acc[3][q]);
             acc[0][q] = acc[1][q] = acc[2][q] = acc[3][q] = 0.f;
         }
     };
 
     if (alive && ncl > 0) {
+        // prefetch distance = number of stages: unit n lives in stage n % NS,
+        // and the stage is refilled with unit n + NS once unit n is in registers
         UnitPos ci, li;
         ci.start(warp, ncl);
         li = ci;
-        issue(0, li);
-        li.advance(ncl);
-        issue(1, li);
-        li.advance(ncl);
+        for (int k = 0; k < NS; ++k) {
+            issue(k, li);
+            li.advance(ncl);
+        }
         int cur_tile = ci.tl;
         for (int n = 0; ci.tl < ntile; ++n) {
             if (ci.tl != cur_tile) {
                 flush(cur_tile);
                 cur_tile = ci.tl;
             }
-            const int st = n & 1;
-            const bool ok = mbar_wait_bounded(smem_addr(&fullbar[warp][st]), (n >> 1) & 1);
-            if (!__all_sync(0xffffffffu, ok)) break;
+            const int st = NS == 2 ? (n & 1) : 0;
+            const bool ok = mbar_wait_bounded(smem_addr(&fullbar[warp][st]), NS == 2 ? ((n >> 1) & 1) : (n & 1));
+            if (!__all_sync(0xffffffffu, ok)) {
+                // units n .. n+NS-1 may still have copies in flight: give each one
+                // more bounded wait before leaving the loop
+                UnitPos pend = ci;
+                for (int k = 0; k < NS && pend.tl < ntile; ++k) {
+                    const int nn = n + k;
+                    mbar_wait_bounded(smem_addr(&fullbar[warp][NS == 2 ? (nn & 1) : 0]),
+                                      NS == 2 ? ((nn >> 1) & 1) : (nn & 1));
+                    pend.advance(ncl);
+                }
+                break;
+            }
             // this lane's 52-byte slices of rows g and g+8
             const uint32_t *s0 = reinterpret_cast<const uint32_t *>(my_stages + st * kStageBytes + g * kChunkBytes + 52 * t);
             const uint32_t *s1 = s0 + 8 * kChunkBytes / 4;
@@ -257,9 +281,9 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_t5_kernel(const T5Params p)
                 wa[q] = s0[q];
                 wb[q] = s1[q];
             }
+            fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) fence_proxy_async_smem();
-            issue(n + 2, li);
+            issue(n + NS, li);
             li.advance(ncl);
 
             // scales (and biases) of this slice's groups, rows g and g+8
@@ -272,11 +296,20 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_t5_kernel(const T5Params p)
                 const bool rok = row < p.N;
                 const __half *sp = p.scales + (long long)row * p.G + gslice;
                 const __half *bp = (HAS_BIAS ? p.biases : p.scales) + (long long)row * p.G + gslice;
+                uint32_t sw[2] = {0u, 0u}, bw[2] = {0u, 0u};
+                if (Ge::NG == 4) {  // 4 halves, 8-byte aligned (G and the slice start are multiples of 4)
+                    const uint2 a = ld_stream_v2_if(sp, rok);
+                    sw[0] = a.x; sw[1] = a.y;
+                    if (HAS_BIAS) { const uint2 b2 = ld_stream_v2_if(bp, rok); bw[0] = b2.x; bw[1] = b2.y; }
+                } else {  // 2 halves, 4-byte aligned
+                    sw[0] = ld_u32_if(sp, rok);
+                    if (HAS_BIAS) bw[0] = ld_u32_if(bp, rok);
+                }
 #pragma unroll
                 for (int q = 0; q < Ge::NG; ++q) {
-                    sv[rr][q] = rok ? __half_as_ushort(sp[q]) : (uint16_t)0;
-                    const uint16_t bq = rok ? __half_as_ushort(bp[q]) : (uint16_t)0;
-                    bv[rr][q] = HAS_BIAS ? bq : __half_as_ushort(sym_bias(__ushort_as_half(bq), p.ratio));
+                    sv[rr][q] = (uint16_t)(sw[q >> 1] >> (16 * (q & 1)));
+                    bv[rr][q] = HAS_BIAS ? (uint16_t)(bw[q >> 1] >> (16 * (q & 1)))
+                                         : __half_as_ushort(sym_bias(__ushort_as_half(sv[rr][q]), p.ratio));
                 }
             }
             // per pair-block beta: s2 = (s[2b], s[2b+1]) and c_d = -2^(10-2d) * s2
@@ -295,43 +328,48 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_t5_kernel(const T5Params p)
                            fabsf(__half2float(__ushort_as_half(sv[rr][2 * be + 1]))) < 63.f;
                 }
             const bool all_fast = __all_sync(0xffffffffu, fast);
-            const uint2 *bq = Bs + ((size_t)ci.cl * kMmas * M + g) * 4 + t;
+            const uint2 *bq = Bs + ((size_t)(ci.cl * M + g) * 4 + t) * kMmas;
 
+            auto pairs = [&](auto fast_tag) {
+                constexpr bool kFast = decltype(fast_tag)::value;
 #pragma unroll
-            for (int jp = 0; jp < 13; ++jp) {
-                uint32_t A0[10], A1[10];
+                for (int jp = 0; jp < 13; ++jp) {
+                    uint32_t A0[10], A1[10];
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int j = 2 * jp + jj;
-                    const int oa = Ge::byte_a(j), ob = oa + B;
-                    const int be = Ge::beta(j);
-                    const uint32_t la0 = lut[__byte_perm(wa[oa >> 2], 0, 0x4440 | (oa & 3))];
-                    const uint32_t lb0 = lut[__byte_perm(wa[ob >> 2], 0, 0x4440 | (ob & 3))];
-                    const uint32_t la1 = lut[__byte_perm(wb[oa >> 2], 0, 0x4440 | (oa & 3))];
-                    const uint32_t lb1 = lut[__byte_perm(wb[ob >> 2], 0, 0x4440 | (ob & 3))];
-                    const uint32_t v0 = mad_u32(lb0, 65536u, la0);
-                    const uint32_t v1 = mad_u32(lb1, 65536u, la1);
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int j = 2 * jp + jj;
+                        const int oa = Ge::byte_a(j), ob = oa + B;
+                        const int be = Ge::beta(j);
+                        const uint32_t la0 = lut[__byte_perm(wa[oa >> 2], 0, 0x4440 | (oa & 3))];
+                        const uint32_t lb0 = lut[__byte_perm(wa[ob >> 2], 0, 0x4440 | (ob & 3))];
+                        const uint32_t la1 = lut[__byte_perm(wb[oa >> 2], 0, 0x4440 | (oa & 3))];
+                        const uint32_t lb1 = lut[__byte_perm(wb[ob >> 2], 0, 0x4440 | (ob & 3))];
+                        const uint32_t v0 = mad_u32(lb0, 65536u, la0);
+                        const uint32_t v1 = mad_u32(lb1, 65536u, la1);
 #pragma unroll
-                    for (int d = 0; d < 5; ++d) {
-                        const uint32_t mask = 0x00030003u << (2 * d);
-                        const uint32_t h0 = (v0 & mask) | mg[d];
-                        const uint32_t h1 = (v1 & mask) | mg[d];
-                        if (all_fast) {
-                            A0[5 * jj + d] = hfma2(h0, s2[0][be], cst[0][be][d]);
-                            A1[5 * jj + d] = hfma2(h1, s2[1][be], cst[1][be][d]);
-                        } else {
-                            A0[5 * jj + d] = hmul2(hsub2(h0, mg[d]), s2[0][be]);
-                            A1[5 * jj + d] = hmul2(hsub2(h1, mg[d]), s2[1][be]);
+                        for (int d = 0; d < 5; ++d) {
+                            const uint32_t mask = 0x00030003u << (2 * d);
+                            const uint32_t h0 = (v0 & mask) | mg[d];
+                            const uint32_t h1 = (v1 & mask) | mg[d];
+                            if (kFast) {
+                                A0[5 * jj + d] = hfma2(h0, s2[0][be], cst[0][be][d]);
+                                A1[5 * jj + d] = hfma2(h1, s2[1][be], cst[1][be][d]);
+                            } else {
+                                A0[5 * jj + d] = hmul2(hsub2(h0, mg[d]), s2[0][be]);
+                                A1[5 * jj + d] = hmul2(hsub2(h1, mg[d]), s2[1][be]);
+                            }
                         }
                     }
-                }
 #pragma unroll
-                for (int q = 0; q < 5; ++q) {
-                    const int i = 5 * jp + q;
-                    const uint2 b = bq[(size_t)i * M * 4];
-                    mma16816(acc[i & 3], A0[2 * q], A1[2 * q], A0[2 * q + 1], A1[2 * q + 1], b.x, b.y);
+                    for (int q = 0; q < 5; ++q) {
+                        const int i = 5 * jp + q;
+                        const uint2 b = bq[i];
+                        mma16816(acc[i & 3], A0[2 * q], A1[2 * q], A0[2 * q + 1], A1[2 * q + 1], b.x, b.y);
+                    }
                 }
-            }
+            };
+            if (all_fast) pairs(std::true_type{});
+            else pairs(std::false_type{});
             // bias term
             const uint2 *sq = SxB + ((size_t)ci.cl * Ge::NB * M + g) * 4 + t;
 #pragma unroll
@@ -347,11 +385,11 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_t5_kernel(const T5Params p)
     __syncthreads();
 
     // ---- reduce: warps (fixed order), then cluster ranks (fixed order) ----------
-    const int nout = ntile * 128;
+    const int nout = ntile * 16 * M;
     for (int e = tid; e < nout; e += kThreads) {
         float v = 0.f;
-        for (int w_ = 0; w_ < kWarps; ++w_) v += accW[(size_t)w_ * p.Tc * 128 + e];
-        if (S > 1) st_cluster_f32(smem_addr(accC + (size_t)rank * p.Tc * 128 + e), 0, v);
+        for (int w_ = 0; w_ < kWarps; ++w_) v += accW[(size_t)w_ * p.Tc * 16 * M + e];
+        if (S > 1) st_cluster_f32(smem_addr(accC + (size_t)rank * p.Tc * 16 * M + e), 0, v);
         else accC[e] = v;
     }
     if (S > 1) {
@@ -360,12 +398,12 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_t5_kernel(const T5Params p)
     } else {
         __syncthreads();
     }
-    for (int e = tid; e < ntile * 16 * M; e += kThreads) {
+    for (int e = tid; e < nout; e += kThreads) {
         const int tl = e / (16 * M), r = (e / M) % 16, m = e % M;
         const int n = (tile0 + tl) * 16 + r;
         if (n >= p.N) continue;
         float v = 0.f;
-        for (int q = 0; q < S; ++q) v += accC[((size_t)q * p.Tc + tl) * 128 + r * 8 + m];
+        for (int q = 0; q < S; ++q) v += accC[(size_t)q * p.Tc * 16 * M + e];
         p.out[(size_t)m * p.N + n] = __float2half_rn(v);
     }
 }
@@ -373,18 +411,19 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_t5_kernel(const T5Params p)
 // ---- host side -----------------------------------------------------------------
 
 struct Plan {
-    int S, Tc, Cs, R;
+    int S, Tc, Cs, R, NS;
     size_t smem;
 };
 
-size_t smem_bytes(int gs, int M, int Cs, int Tc, int S)
+size_t smem_bytes(int gs, int M, int Cs, int Tc, int S, int NS)
 {
     const int nb = gs == 64 ? 2 : 1;
-    size_t b = 1024 + (size_t)kStageArea;
-    b += ((size_t)Cs * kMmas * M * 4 + 32) * sizeof(uint2);
+    size_t b = 1024 + (size_t)kWarps * NS * kStageBytes;
+    b += ((size_t)Cs * M * 4 * kMmas + 8 * 4 * kMmas) * sizeof(uint2);
     b += ((size_t)Cs * nb * M * 4 + 32) * sizeof(uint2);
-    b += (size_t)(kWarps + S) * Tc * 128 * sizeof(float);
-    return b;
+    const size_t raw = (size_t)M * Cs * kChunkCodes * sizeof(__half);
+    const size_t accs = (size_t)(kWarps + S) * Tc * 16 * M * sizeof(float);
+    return b + (raw > accs ? raw : accs);
 }
 
 using OccFn = int (*)(int S, size_t smem);
@@ -393,23 +432,31 @@ bool make_plan(int gs, int M, int tiles, int chunks, int sms, OccFn occ, Plan &b
 {
     double best_cost = 1e30;
     bool found = false;
-    for (int S = 1; S <= 8 && S <= chunks; ++S) {
-        const int Cs = (chunks + S - 1) / S;
-        if ((S - 1) * Cs >= chunks) continue;
-        if ((size_t)M * Cs * kChunkCodes * 2 > (size_t)kStageArea) continue;  // raw x fits the ring
-        for (int Tc = 1; Tc <= kMaxTc; ++Tc) {
-            const int R = (tiles + Tc - 1) / Tc;
-            const size_t sm = smem_bytes(gs, M, Cs, Tc, S);
-            if (sm > kSmemBudget) continue;
-            const int slots = S == 1 ? 2 * sms : occ(S, sm);
-            if (slots <= 0) continue;
-            const int waves = (R + slots - 1) / slots;
-            const int per_warp = (Cs * Tc + kWarps - 1) / kWarps;
-            const double cost = (double)waves * (per_warp + 1.5) + 0.01 * S;
-            if (cost < best_cost - 1e-9) {
-                best_cost = cost;
-                best = Plan{S, Tc, Cs, R, sm};
-                found = true;
+    // testing knob: BQD_T5_STAGES=1|2 restricts the stage count
+    const char *knob = getenv("BQD_T5_STAGES");
+    const int ns_only = knob ? atoi(knob) : 0;
+    for (int NS = 2; NS >= 1; --NS) {
+        if (ns_only && NS != ns_only) continue;
+        for (int S = 1; S <= 8 && S <= chunks; ++S) {
+            const int Cs = (chunks + S - 1) / S;
+            if ((S - 1) * Cs >= chunks) continue;
+            for (int Tc = 1; Tc <= kMaxTc; ++Tc) {
+                const int R = (tiles + Tc - 1) / Tc;
+                const size_t sm = smem_bytes(gs, M, Cs, Tc, S, NS);
+                if (sm > kSmemBudget) continue;
+                const int slots = S == 1 ? 2 * sms : occ(S, sm);
+                if (slots <= 0) continue;
+                const int waves = (R + slots - 1) / slots;
+                const int per_warp = (Cs * Tc + kWarps - 1) / kWarps;
+                // a unit is the bulk of the time; the prologue (x staging and
+                // permute) costs ~0.15 unit per chunk and activation row plus a
+                // copy round trip; a single stage exposes some copy latency
+                const double cost = (double)waves * (per_warp * (NS == 2 ? 1.0 : 1.15) + 1.0 + 0.15 * Cs * M) + 0.01 * S;
+                if (cost < best_cost - 1e-9) {
+                    best_cost = cost;
+                    best = Plan{S, Tc, Cs, R, NS, sm};
+                    found = true;
+                }
             }
         }
     }
@@ -517,7 +564,10 @@ int launch_qmv_t5(const QmvArgs &a, cudaStream_t s)
         p.M = M;
         p.x = a.x + m0 * a.K;
         p.out = a.out + m0 * a.N;
-        p.S = pl.S; p.Tc = pl.Tc; p.Cs = pl.Cs;
+        p.S = pl.S; p.Tc = pl.Tc; p.Cs = pl.Cs; p.NS = pl.NS;
+        if (getenv("BQD_DEBUG_PLAN"))
+            fprintf(stderr, "bqd %s plan: N=%d K=%d M=%d gs=%d -> S=%d Tc=%d Cs=%d R=%d NS=%d grid=%d smem=%zu\n", "t5",
+                    p.N, p.K, M, a.gs, pl.S, pl.Tc, pl.Cs, pl.R, pl.NS, pl.R * pl.S, pl.smem);
         int st;
         if (a.gs == 64) st = hb ? launch_t<64, true>(p, pl, s) : launch_t<64, false>(p, pl, s);
         else st = hb ? launch_t<128, true>(p, pl, s) : launch_t<128, false>(p, pl, s);

@@ -76,6 +76,15 @@ def test_tensor_core_paths_forced(fmt, gs, sym):
         run_case(p, "mma")
 
 
+@pytest.mark.parametrize("stages", ["1", "2"])
+@pytest.mark.parametrize("gs", [64, 128])
+def test_t5_stage_ring_depths(stages, gs, monkeypatch):
+    """The t5 kernel's weight ring with one and with two stages per warp."""
+    monkeypatch.setenv("BQD_T5_STAGES", stages)
+    for M, N, K in [(1, 300, 3072), (5, 1000, 2048), (8, 40, 5120)]:
+        run_case(synth.problem(T5, M, N, K, gs, sym=True), "mma")
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_config1_all_rows(kernel):
     """1-bit, M=1, N=256, K=512, gs=64, seed 0."""
