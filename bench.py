@@ -360,7 +360,8 @@ def run_case(spec: str, sets: int, reps: int = 64):
     e1.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / reps
     nb = call_bytes(fmt, sym or fmt == T5, M, N, K, gs)
-    print(json.dumps({"case": spec, "us_per_call_eager": us, "gbs": nb / (us * 1e-6) / 1e9}), flush=True)
+    print(json.dumps({"case": spec, "us_per_call_eager": us, "gbs": nb / (us * 1e-6) / 1e9,
+                      "tflops": 2.0 * M * N * K / (us * 1e-6) / 1e12}), flush=True)
     return 0
 
 

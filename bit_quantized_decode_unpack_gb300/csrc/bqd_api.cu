@@ -99,6 +99,11 @@ static int qmv_common(const void *x, const void *w, const void *scales, const vo
 
     const int force = forced_kernel();
     if (force != 1) {
+        // t5 prefill (M > 16): fused unpack + tcgen05 matrix product
+        if (format == BQD_FMT_T5 && M > 16) {
+            int st = launch_qmm_t5(a, s);
+            if (st != BQD_ERR_UNSUPPORTED || force == 2) return st;
+        }
         int st = format == BQD_FMT_T5 ? launch_qmv_t5(a, s) : launch_qmv_mma(a, s);
         if (st != BQD_ERR_UNSUPPORTED || force == 2) return st;
     }
@@ -192,10 +197,12 @@ extern "C" int bqd_detect_sym(const void *scales, const void *biases, int64_t N,
 extern "C" int bqd_device_status(bqd_stream_t stream)
 {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return BQD_ERR_CUDA;
-    unsigned int n1 = 0, n2 = 0;
+    unsigned int n1 = 0, n2 = 0, n3 = 0;
     int st = take_qmv_mma_timeouts(&n1);
     if (st != BQD_OK) return st;
     st = take_qmv_t5_timeouts(&n2);
     if (st != BQD_OK) return st;
-    return (n1 || n2) ? BQD_ERR_TIMEOUT : BQD_OK;
+    st = take_qmm_timeouts(&n3);
+    if (st != BQD_OK) return st;
+    return (n1 || n2 || n3) ? BQD_ERR_TIMEOUT : BQD_OK;
 }

@@ -37,6 +37,8 @@ int launch_qmv_generic(const QmvArgs &a, cudaStream_t s);
 int launch_qmv_mma(const QmvArgs &a, cudaStream_t s);
 // Tensor-core decode path for t5 weights (K a multiple of 1024); same contract.
 int launch_qmv_t5(const QmvArgs &a, cudaStream_t s);
+// t5 prefill matrix product on tcgen05 tensor cores (meant for M > 16).
+int launch_qmm_t5(const QmvArgs &a, cudaStream_t s);
 
 int launch_pack(const uint8_t *codes, int64_t N, int64_t K, int fmt, int gs,
                 uint8_t *w, cudaStream_t s);
@@ -61,6 +63,7 @@ inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? BQD_OK : BQD_E
 // decode kernel; BQD_OK / BQD_ERR_CUDA.
 int take_qmv_mma_timeouts(unsigned int *count);
 int take_qmv_t5_timeouts(unsigned int *count);
+int take_qmm_timeouts(unsigned int *count);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

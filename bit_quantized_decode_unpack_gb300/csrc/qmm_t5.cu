@@ -1,0 +1,510 @@
+// t5 prefill matrix product on the 5th-generation tensor cores (tcgen05).
+//
+// Page: "oMLX Bonsai 自定义内核:Qwen 系列快速 QMV 路径完整解析", §二.3: for long
+// prefill (M > 16) t5 weights go through a fused "unpack + matrix multiply"
+// kernel (bonsai_t5_qmm) that reads every t5 byte once.
+//
+//   Y[m, n] = sum_k X[m, k] * W[n, k],  W[n, k] = fp16(s[n,g] * t[n,k] + b[n,g])
+//   (sym: b = fp16(-ratio * s), default ratio 1 -> W = s*(t-1), exact in fp16)
+//
+// One CTA owns 128 weight rows x BX activation rows (BX = 32, 64 or 128) and a
+// range of K groups.  When the (weight, activation) tiles are too few to fill
+// the GPU, the K range is split over the CTAs of a cluster and the partial
+// tiles are reduced through distributed shared memory (no global scratch).
+//
+// Roles (192 threads):
+//   warps 0-3  decode: thread r owns weight row n0+r.  Per K step (one group
+//              of gs codes) it loads the row's t5 bytes, decodes them with a
+//              shared byte->trits table, forms the fp16 weights (magic-exponent
+//              LOP3 + HFMA2 gives s*t exactly, then + b) and stores them into
+//              the stage's A tile in the tcgen05 K-major 128-byte-swizzled
+//              layout.  After the K loop the same warps drain the TMEM
+//              accumulator (tcgen05.ld) and store Y.
+//   warp 4     allocates TMEM; lane 0 issues tcgen05.mma (kind::f16, M=128,
+//              N=BX, K=16, fp32 accumulation in TMEM) and tcgen05.commit, which
+//              frees a stage once its MMAs have completed.
+//   warp 5     lane 0 loads X tiles with TMA (cp.async.bulk.tensor, 128-byte
+//              swizzle, zero fill past M).
+// Every mbarrier wait is bounded; on expiry the CTA stops issuing work, drains
+// what it issued (bounded), passes its remaining barriers and frees TMEM; the
+// expiry is counted for bqd_device_status.
+#include <cudaTypedefs.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "bqd_internal.cuh"
+#include "qmv_common.cuh"
+
+namespace bqd {
+namespace {
+
+using namespace qmvdev;
+
+constexpr int kThreadsQ = 192;
+constexpr int kMaxStagesQ = 8;
+constexpr size_t kQmmSmemMax = 220 * 1024;
+
+__device__ unsigned int g_qmm_timeouts = 0;
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < kWaitSpins; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    atomicAdd(&g_qmm_timeouts, 1u);
+    return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// ---- tcgen05 wrappers ------------------------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand with 128-byte swizzle:
+// start address >> 4, leading byte offset (unused for swizzled K-major, 1),
+// stride byte offset 1024 >> 4 (8-row groups of 128-byte rows), descriptor
+// version 1 (bit 46), layout type SWIZZLE_128B (2, bits 61-63).  Stepping
+// K by 16 fp16 elements moves the start address by 32 bytes.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B f16 (0),
+// both K-major (bits 15, 16 = 0), N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N)
+{
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+struct QmmParams {
+    const uint8_t *w;
+    const __half *scales;
+    const __half *biases;
+    __half *out;
+    float ratio;
+    int M, N, K, G;
+    long long row_bytes;
+    int bx, S, gpr, stages;  // gpr: K groups per cluster rank
+    uint32_t zero;           // always 0: keeps the magic constants in registers
+};
+
+// byte offset of 16-byte chunk c of row r inside one 128-row x 64-code
+// sub-tile (128-byte rows, 8-row groups of 1024 bytes, chunk index ^ row%8)
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c)
+{
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+template <int GS>
+__global__ void __launch_bounds__(kThreadsQ, 1)
+qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
+{
+    constexpr int B = GS == 64 ? 13 : 26;  // t5 bytes per group
+    constexpr int NSUB = GS / 64;          // 64-code sub-tiles per K step
+    constexpr int A_BYTES = 128 * GS * 2;  // A tile per stage
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t x_full[kMaxStagesQ], a_full[kMaxStagesQ], empty_bar[kMaxStagesQ], done_bar;
+    __shared__ uint32_t tmem_base;
+    __shared__ uint32_t lut[256];
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = p.S;
+    const int rank = S > 1 ? (int)cluster_ctarank() : 0;
+    const int tile = blockIdx.x / S;
+    const int n_tiles = (p.N + 127) / 128;
+    const int nt = tile % n_tiles, mt = tile / n_tiles;
+    const int n0 = nt * 128, m0 = mt * p.bx;
+    const int g_lo = rank * p.gpr;
+    const int g_hi = min(p.G, g_lo + p.gpr);
+    const int steps = max(0, g_hi - g_lo);
+    const int NST = p.stages;
+    const uint32_t X_BYTES = (uint32_t)p.bx * GS * 2;
+
+    // 1024-byte aligned stage ring: [A tile | X tile] per stage
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t stage_bytes = A_BYTES + X_BYTES;
+
+    for (int q = tid; q < 256; q += kThreadsQ) {
+        int v = q, e = 0;
+        if (v < 243)
+            for (int d = 0; d < 5; ++d) {
+                e |= (v % 3) << (2 * d);
+                v /= 3;
+            }
+        lut[q] = (uint32_t)e;
+    }
+    if (tid == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(smem_addr(&x_full[s]), 1);
+            mbar_init(smem_addr(&a_full[s]), 128);
+            mbar_init(smem_addr(&empty_bar[s]), 1);
+        }
+        mbar_init(smem_addr(&done_bar), 1);
+        abort_flag = 0;
+    }
+    if (warp == 4) tmem_alloc(smem_addr(&tmem_base), (uint32_t)p.bx);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    pdl_wait();
+
+    if (warp == 5) {
+        // ---- X producer ---------------------------------------------------------
+        if (lane == 0) {
+            int issued = 0;
+            for (int it = 0; it < steps; ++it) {
+                const int s = it % NST;
+                if (it >= NST && !wait_bounded(smem_addr(&empty_bar[s]), ((it / NST) - 1) & 1)) {
+                    abort_flag = 1;
+                    break;
+                }
+                const uint32_t bar = smem_addr(&x_full[s]);
+                mbar_arrive_expect_tx(bar, X_BYTES);
+                const int k = (g_lo + it) * GS;
+                uint8_t *xt = smem + (size_t)s * stage_bytes + A_BYTES;
+                for (int sub = 0; sub < NSUB; ++sub)
+                    tma_load_2d(smem_addr(xt + sub * p.bx * 128), &xmap, k + 64 * sub, m0, bar);
+                issued = it + 1;
+            }
+            if (abort_flag) {
+                // drain the copies this CTA issued (bounded) before anyone leaves
+                for (int it = max(0, issued - NST); it < issued; ++it)
+                    wait_bounded(smem_addr(&x_full[it % NST]), (it / NST) & 1);
+            }
+        }
+    } else if (warp == 4) {
+        // ---- MMA issuer -----------------------------------------------------------
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(128, p.bx);
+            bool ok = true;
+            for (int it = 0; it < steps; ++it) {
+                const int s = it % NST;
+                const uint32_t par = (it / NST) & 1;
+                ok = wait_bounded(smem_addr(&x_full[s]), par) && wait_bounded(smem_addr(&a_full[s]), par);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t a0 = smem_addr(smem + (size_t)s * stage_bytes);
+                const uint32_t x0 = a0 + A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < GS / 16; ++kk) {
+                    const int sub = kk >> 2, within = kk & 3;
+                    const uint64_t ad = sw128_desc(a0 + sub * 16384 + within * 32);
+                    const uint64_t bd = sw128_desc(x0 + sub * p.bx * 128 + within * 32);
+                    tc_mma(tmem, ad, bd, idesc, (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(smem_addr(&empty_bar[s]));
+            }
+            if (!ok) abort_flag = 1;
+            tc_commit(smem_addr(&done_bar));  // arrives once every issued MMA has completed
+        }
+    } else {
+        // ---- decode warps: weight row n0 + tid ---------------------------------------
+        const int r = tid;
+        const int row = n0 + r;
+        const bool rok = row < p.N;
+        const uint8_t *wrow = p.w + (long long)(rok ? row : 0) * p.row_bytes;
+        const __half *srow = p.scales + (long long)(rok ? row : 0) * p.G;
+        const __half *brow = p.biases ? p.biases + (long long)(rok ? row : 0) * p.G : nullptr;
+        uint32_t mg[5];
+#pragma unroll
+        for (int d = 0; d < 5; ++d) mg[d] = magic(2 * d) ^ p.zero;
+        for (int it = 0; it < steps; ++it) {
+            const int s = it % NST;
+            if (it >= NST && !wait_bounded(smem_addr(&empty_bar[s]), ((it / NST) - 1) & 1)) {
+                abort_flag = 1;
+                break;
+            }
+            const int g = g_lo + it;
+            // the group's bytes, via aligned 32-bit loads realigned with funnel
+            // shifts (row_bytes is a multiple of 16 here)
+            constexpr int NW = (B + 3 + 3) / 4;
+            uint32_t bytes_w[NW];
+            {
+                const long long off = (long long)g * B;
+                const long long aoff = off & ~3LL;
+                const uint32_t *base = reinterpret_cast<const uint32_t *>(wrow + aoff);
+                const int sh = (int)(off & 3) * 8;
+                uint32_t raw[NW + 1];
+#pragma unroll
+                for (int q = 0; q <= NW; ++q) raw[q] = (rok && aoff + 4 * q < p.row_bytes) ? base[q] : 0u;
+#pragma unroll
+                for (int q = 0; q < NW; ++q) bytes_w[q] = __funnelshift_r(raw[q], raw[q + 1], sh);
+            }
+            const uint16_t sb = rok ? __half_as_ushort(srow[g]) : (uint16_t)0;
+            const uint16_t bb = rok ? (brow ? __half_as_ushort(brow[g])
+                                            : __half_as_ushort(sym_bias(__ushort_as_half(sb), p.ratio)))
+                                    : (uint16_t)0;
+            const uint32_t s2 = dup_half(sb), b2 = dup_half(bb);
+            // constants -2^(10-2d)*s stay finite for |s| < 63; else the exact
+            // (magic - offset) * s form is used
+            const bool fast = fabsf(__half2float(__ushort_as_half(sb))) < 63.f;
+            uint32_t c[5];
+#pragma unroll
+            for (int d = 0; d < 5; ++d)
+                c[d] = hmul2(s2, dup_half(__half_as_ushort(__float2half_rn(-(float)(1024 >> (2 * d))))));
+            auto wv = [&](uint32_t field_word, uint32_t mask, int d) -> uint32_t {
+                const uint32_t h = (field_word & mask) | mg[d];
+                const uint32_t ts = fast ? hfma2(h, s2, c[d]) : hmul2(hsub2(h, mg[d]), s2);  // t*s, exact
+                return hadd2(ts, b2);
+            };
+            auto lut_of = [&](int j) -> uint32_t { return lut[__byte_perm(bytes_w[j >> 2], 0, 0x4440 | (j & 3))]; };
+            // codes of the group in order, two per 32-bit word (code 2i low, 2i+1 high)
+            uint32_t hv[GS / 2];
+#pragma unroll
+            for (int j = 0; j + 1 < B; j += 2) {
+                const uint32_t L0 = lut_of(j), L1 = lut_of(j + 1);
+                const uint32_t u = L0 * 16385u;      // fields of byte j, also shifted by 14
+                const uint32_t u2 = L0 + (L1 << 24);  // (trit 4 of byte j, trit 0 of byte j+1) at bit 8
+                const uint32_t u3 = L1 * 16385u;     // fields of byte j+1, also shifted by 14
+                const int k = 5 * j;                 // first code of byte j (even)
+                hv[k / 2] = wv(u, 0x00030003u, 0);
+                hv[k / 2 + 1] = wv(u, 0x00300030u, 2);
+                hv[k / 2 + 2] = wv(u2, 0x03000300u, 4);
+                if (k / 2 + 3 < GS / 2) hv[k / 2 + 3] = wv(u3, 0x000C000Cu, 1);
+                if (k / 2 + 4 < GS / 2) hv[k / 2 + 4] = wv(u3, 0x00C000C0u, 3);
+            }
+            if (B & 1) {  // gs=64: byte 12 holds codes 60..63
+                const uint32_t u = lut_of(B - 1) * 16385u;
+                hv[GS / 2 - 2] = wv(u, 0x00030003u, 0);
+                hv[GS / 2 - 1] = wv(u, 0x00300030u, 2);
+            }
+            // store into the stage's A tile (K-major, 128-byte swizzle)
+            uint8_t *at = smem + (size_t)s * stage_bytes;
+#pragma unroll
+            for (int chunk = 0; chunk < GS / 8; ++chunk) {
+                uint4 v = make_uint4(hv[4 * chunk], hv[4 * chunk + 1], hv[4 * chunk + 2], hv[4 * chunk + 3]);
+                if (!rok) v = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(at + (chunk >> 3) * 16384 + sw128_offset(r, chunk & 7)) = v;
+            }
+            fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+            mbar_arrive(smem_addr(&a_full[s]));
+        }
+    }
+
+    // ---- epilogue ----------------------------------------------------------------
+    __syncthreads();
+    if (warp < 4 && steps > 0) wait_bounded(smem_addr(&done_bar), 0);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const bool ok_all = !abort_flag;
+    float *red = reinterpret_cast<float *>(smem);  // split-K partials reuse rank 0's stage ring
+    if (S > 1) cluster_sync();                     // every rank's MMAs are complete
+    const int r = (warp & 3) * 32 + lane;
+    const int row = n0 + r;
+    if (warp < 4 && S > 1 && rank != 0 && steps > 0) {
+        for (int c0 = 0; c0 < p.bx; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+            float *dst = red + ((size_t)(rank - 1) * 128 + r) * p.bx + c0;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) st_cluster_f32(smem_addr(dst + q), 0, __uint_as_float(v[q]));
+        }
+    }
+    if (S > 1) cluster_sync();
+    if (warp < 4 && rank == 0 && ok_all) {
+        for (int c0 = 0; c0 < p.bx; c0 += 32) {
+            uint32_t v[32];
+            if (steps > 0) {
+                tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] = 0u;
+            }
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                float acc = __uint_as_float(v[q]);
+                for (int rr = 1; rr < S; ++rr)
+                    if (rr * p.gpr < p.G) acc += red[((size_t)(rr - 1) * 128 + r) * p.bx + c0 + q];
+                const int m = m0 + c0 + q;
+                if (row < p.N && m < p.M) p.out[(size_t)m * p.N + row] = __float2half_rn(acc);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) tmem_dealloc(tmem, (uint32_t)p.bx);
+}
+
+// ---- host side -------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+template <int GS>
+int launch_gs(const QmmParams &p, const CUtensorMap &map, int tiles, size_t smem, cudaStream_t s)
+{
+    auto kern = qmm_t5_kernel<GS>;
+    static int configured_dev[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured_dev[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQmmSmemMax) != cudaSuccess)
+            return BQD_ERR_CUDA;
+        configured_dev[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles * p.S);
+    cfg.blockDim = dim3(kThreadsQ);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (p.S > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = p.S;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, map, p) == cudaSuccess ? BQD_OK : BQD_ERR_CUDA;
+}
+
+}  // namespace
+
+int take_qmm_timeouts(unsigned int *count)
+{
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_qmm_timeouts, sizeof(v)) != cudaSuccess) return BQD_ERR_CUDA;
+    if (v && cudaMemcpyToSymbol(g_qmm_timeouts, &zero, sizeof(zero)) != cudaSuccess) return BQD_ERR_CUDA;
+    *count = v;
+    return BQD_OK;
+}
+
+int launch_qmm_t5(const QmvArgs &a, cudaStream_t s)
+{
+    if (a.fmt != BQD_FMT_T5) return BQD_ERR_UNSUPPORTED;
+    if (a.row_bytes % 16 != 0) return BQD_ERR_UNSUPPORTED;  // aligned 32-bit byte loads stay inside a row
+    if (a.K > (int64_t)1 << 30 || a.N > (int64_t)1 << 30 || a.M > (int64_t)1 << 30) return BQD_ERR_UNSUPPORTED;
+    auto enc = encode_fn();
+    if (!enc) return BQD_ERR_UNSUPPORTED;
+    QmmParams p;
+    p.w = a.w; p.scales = a.scales; p.biases = a.biases; p.out = a.out; p.ratio = a.ratio;
+    p.M = (int)a.M; p.N = (int)a.N; p.K = (int)a.K; p.G = (int)a.G;
+    p.row_bytes = a.row_bytes;
+    p.zero = 0;
+    p.bx = a.M <= 32 ? 32 : (a.M <= 64 ? 64 : 128);
+    const int n_tiles = (p.N + 127) / 128, m_tiles = (p.M + p.bx - 1) / p.bx;
+    const int tiles = n_tiles * m_tiles;
+    const int sms = sm_count();
+    const size_t per_stage = (size_t)128 * a.gs * 2 + (size_t)p.bx * a.gs * 2;
+    p.stages = (int)((kQmmSmemMax - 1024) / per_stage);
+    if (p.stages > kMaxStagesQ) p.stages = kMaxStagesQ;
+    if (p.stages < 2) return BQD_ERR_UNSUPPORTED;
+    // split K over a cluster while that fills more SMs (one CTA per SM), each
+    // rank keeps >= 4 groups, and the (S-1) fp32 partial tiles fit the ring
+    int S = 1;
+    while (S < 8 && tiles * (S + 1) <= sms && p.G >= 4 * (S + 1) &&
+           (size_t)S * 128 * p.bx * 4 <= (size_t)p.stages * per_stage)
+        ++S;
+    p.S = S;
+    p.gpr = (p.G + S - 1) / S;
+    const size_t smem = (size_t)p.stages * per_stage + 1024;
+
+    CUtensorMap map;
+    cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+    cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)p.bx};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(a.x), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return BQD_ERR_CUDA;
+    if (getenv("BQD_DEBUG_PLAN"))
+        fprintf(stderr, "bqd qmm plan: M=%d N=%d K=%d gs=%d -> bx=%d tiles=%d S=%d gpr=%d stages=%d smem=%zu\n", p.M,
+                p.N, p.K, a.gs, p.bx, tiles, S, p.gpr, p.stages, smem);
+    return a.gs == 64 ? launch_gs<64>(p, map, tiles, smem, s) : launch_gs<128>(p, map, tiles, smem, s);
+}
+
+}  // namespace bqd
