@@ -310,6 +310,43 @@ def per_call_table(sweep, reps: int = 3):
     return rows
 
 
+QMM_CASES = [(M, N, K) for M in (32, 512, 2048) for (N, K) in [(17408, 5120), (5120, 17408)]]
+
+
+def time_qmm(dev, reps: int = 10):
+    """t5 prefill matrix product (M > 16 -> tcgen05 kernel), gs=128: TFLOP/s
+    per case (2*M*N*K flops), each case over two rotating weight sets."""
+    import torch
+    import bit_quantized_decode_unpack_gb300 as bqd
+    from bit_quantized_decode_unpack_gb300 import synth
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(77)
+    rows, tot_flop, tot_ms = [], 0.0, 0.0
+    for M, N, K in QMM_CASES:
+        W = []
+        for _ in range(2):
+            s_ = synth.torch_scales(gen, N, K // 128, dev)
+            W.append((bqd.pack(synth.torch_codes(gen, T5, N, K, dev), T5, 128), s_))
+        x = synth.torch_activations(gen, M, K, dev)
+        y = torch.empty(M, N, dtype=torch.float16, device=dev)
+        for i in range(3):
+            bqd.qmv(x, W[i % 2][0], W[i % 2][1], None, T5, 128, out=y)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(reps):
+            bqd.qmv(x, W[i % 2][0], W[i % 2][1], None, T5, 128, out=y)
+        e1.record()
+        e1.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        flop = 2.0 * M * N * K
+        rows.append({"M": M, "N": N, "K": K, "us": round(ms * 1e3, 1), "tflops": round(flop / (ms * 1e-3) / 1e12, 1)})
+        tot_flop += flop
+        tot_ms += ms
+        del W, x, y
+    return rows, tot_flop / (tot_ms * 1e-3) / 1e12
+
+
 def kernel_traffic_from_profiles():
     """DRAM-bytes / algorithmic-bytes ratio of the QMV kernels from the committed
     ncu summaries, or None when a kernel source changed since it was taken."""
@@ -450,6 +487,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="two projections only (development)")
     ap.add_argument("--table", type=str, default=None, help="write the per-call table (CSV) here")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-qmm", action="store_true", help="skip the t5 prefill matrix-product timing")
     ap.add_argument("--cpu-rows", type=int, default=0, help="0: sized for ~12 s of oracle work")
     ap.add_argument("--case", type=str, default=None, help="fmt,M,N,K,gs[,sym]: time one configuration")
     args = ap.parse_args()
@@ -526,6 +564,13 @@ def main():
             "gpu_launches": len(sweep.calls) * args.steps,
             "clocks": clocks,
         }
+        if not args.no_qmm:
+            qrows, qagg = time_qmm(dev)
+            tf_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+            line["qmm"] = {"metric": "t5 prefill QMM TFLOP/s (2*M*N*K), gs=128", "value": qagg, "unit": "TFLOP/s",
+                           "cases": qrows,
+                           "roofline": {"bound": "tensor", "achieved": qagg, "peak": tf_peak, "unit": "TFLOP/s",
+                                        "frac": qagg / tf_peak, "peak_source": src + " bf16 burst (fp16 runs at the bf16 rate)"}}
         if not args.no_cpu_baseline:
             import oracle
             oracle.build()
