@@ -35,6 +35,9 @@ int launch_qmv_generic(const QmvArgs &a, cudaStream_t s);
 // Tensor-core decode path; BQD_ERR_UNSUPPORTED when the request is outside
 // its shape/alignment envelope (the caller then uses the generic kernel).
 int launch_qmv_mma(const QmvArgs &a, cudaStream_t s);
+// Tensor-core decode path for 1/2-bit codes fed by a TMA shared-memory ring
+// (K a multiple of 256, 16-byte aligned rows); same contract.
+int launch_qmv_tma(const QmvArgs &a, cudaStream_t s);
 // Tensor-core decode path for t5 weights (K a multiple of 1024); same contract.
 int launch_qmv_t5(const QmvArgs &a, cudaStream_t s);
 // t5 prefill matrix product on tcgen05 tensor cores (meant for M > 16).
@@ -64,6 +67,7 @@ inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? BQD_OK : BQD_E
 int take_qmv_mma_timeouts(unsigned int *count);
 int take_qmv_t5_timeouts(unsigned int *count);
 int take_qmm_timeouts(unsigned int *count);
+int take_qmv_tma_timeouts(unsigned int *count);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

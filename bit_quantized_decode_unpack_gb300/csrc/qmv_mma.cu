@@ -350,6 +350,9 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_mma_kernel(const Params p)
     float *accW = reinterpret_cast<float *>(region);  // [warps][Tc][16][8], after the prologue
     float *accC = accW + (size_t)kWarps * p.Tc * 128;  // [S][Tc][16][8]
     const uint32_t bar = smem_addr(&xbar);
+    // the next kernel may launch now: it only prefetches weights until its
+    // griddepcontrol.wait, which waits for this whole grid
+    pdl_launch_dependents();
     if (tid == 0) mbar_init(bar, 1);
 
     // ---- weights of the first three units: independent of the previous kernel --
@@ -440,7 +443,6 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_mma_kernel(const Params p)
     for (int e = tid; e < kWarps * p.Tc * 128; e += kThreads) accW[e] = 0.f;
     __syncthreads();
     if (S > 1) cluster_sync();  // rank 0's accumulators exist before anyone writes them
-    pdl_launch_dependents();
 
     // ---- main loop: two units in flight while one is computed -------------------
     uint32_t mg[F::kNumPos];

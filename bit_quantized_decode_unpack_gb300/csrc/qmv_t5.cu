@@ -133,6 +133,9 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_t5_kernel(const T5Params p)
         lut[tid] = (uint32_t)e;
     }
     const uint32_t xb = smem_addr(&xbar);
+    // the next kernel may launch now: it only prefetches weights until its
+    // griddepcontrol.wait, which waits for this whole grid
+    pdl_launch_dependents();
     if (tid == 0) mbar_init(xb, 1);
     if (lane == 0)
         for (int st = 0; st < NS; ++st) mbar_init(smem_addr(&fullbar[warp][st]), 1);
@@ -205,7 +208,6 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_t5_kernel(const T5Params p)
     for (int e = tid; e < kWarps * p.Tc * 16 * M; e += kThreads) accW[e] = 0.f;
     __syncthreads();
     if (S > 1) cluster_sync();
-    pdl_launch_dependents();
 
     // ---- per-warp stage ring --------------------------------------------------
     uint8_t *my_stages = stages + (size_t)warp * NS * kStageBytes;

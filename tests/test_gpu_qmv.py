@@ -17,7 +17,7 @@ from _util import assert_within_tolerance, forced_kernel, to_dev
 
 pytestmark = pytest.mark.gpu
 F1, F2, T5 = bqd.FMT_AFFINE1, bqd.FMT_AFFINE2, bqd.FMT_T5
-KERNELS = [None, "generic"]  # None = the dispatcher's choice; "mma" forces the tensor-core paths
+KERNELS = [None, "generic"]  # None = the dispatcher's choice; "mma"/"tma" force the tensor-core paths
 
 
 def run_case(p, kernel=None, rows=None, explicit_ratio=None):
@@ -63,17 +63,49 @@ MMA_SHAPES = [(1, 17, 1024), (2, 300, 2048), (3, 130, 3072), (5, 1000, 1024), (8
               (4, 16, 5120), (6, 1, 1024)]
 
 
-@pytest.mark.parametrize("fmt", [F1, F2, T5])
+@pytest.mark.parametrize("kernel,fmt", [("mma", F1), ("mma", F2), ("mma", T5), ("tma", F1), ("tma", F2)])
 @pytest.mark.parametrize("gs", [64, 128])
 @pytest.mark.parametrize("sym", [False, True])
-def test_tensor_core_paths_forced(fmt, gs, sym):
-    """BQD_FORCE_KERNEL=mma makes an unsupported request an error instead of
-    a fallback, so these cases are known to run on the tensor-core kernels."""
+def test_tensor_core_paths_forced(kernel, fmt, gs, sym):
+    """BQD_FORCE_KERNEL=mma|tma makes an unsupported request an error instead
+    of a fallback, so these cases are known to run on the named kernel."""
     for M, N, K in MMA_SHAPES:
         p = synth.problem(fmt, M, N, K, gs, sym=sym)
         if fmt == T5 and not sym:
             p["biases"] = synth.biases(np.random.default_rng(N), F2, p["scales"])
-        run_case(p, "mma")
+        run_case(p, kernel)
+
+
+# TMA-ring kernel: one 256-code chunk, row blocks of 128 with ragged tails,
+# split-K clusters of several sizes, M up to 8 and two passes for M > 8
+TMA_SHAPES = [(1, 1, 256), (2, 127, 256), (3, 128, 512), (4, 129, 768), (5, 383, 4096), (7, 1024, 5120),
+              (8, 2000, 1280), (9, 200, 2304), (16, 130, 1024), (1, 5120, 17408), (5, 300, 17408)]
+
+
+@pytest.mark.parametrize("fmt", [F1, F2])
+@pytest.mark.parametrize("gs", [64, 128])
+@pytest.mark.parametrize("sym", [False, True])
+def test_tma_kernel_shapes(fmt, gs, sym):
+    for M, N, K in TMA_SHAPES:
+        p = synth.problem(fmt, M, N, K, gs, sym=sym)
+        run_case(p, "tma")
+
+
+@pytest.mark.parametrize("kernel", ["tma", "mma", "generic"])
+@pytest.mark.parametrize("fmt", [F1, F2])
+def test_zero_codes_zero_bias_give_exact_zeros(kernel, fmt):
+    """w = s*0 + 0 everywhere: y is exactly 0 whatever x and s are (the TMA
+    kernel's offset cancellation is exact for code-free groups)."""
+    import torch
+    M, N, K, gs = 5, 300, 2048, 64
+    p = synth.problem(fmt, M, N, K, gs)
+    codes = np.zeros_like(p["codes"])
+    w = bqd.pack(to_dev(codes), fmt, gs)
+    b = torch.zeros((N, K // gs), dtype=torch.float16, device="cuda")
+    with forced_kernel(kernel):
+        y = bqd.qmv(to_dev(p["x"]), w, to_dev(p["scales"]), b, fmt, gs)
+    torch.cuda.synchronize()
+    assert torch.all(y == 0)
 
 
 @pytest.mark.parametrize("stages", ["1", "2"])
@@ -226,6 +258,8 @@ def test_large_scales_take_the_exact_unpack(fmt):
     p["x"] = (p["x"].astype(np.float32) * 1e-3).astype(np.float16)
     run_case(p, "mma")
     run_case(p, None)
+    if fmt != T5:
+        run_case(p, "tma")
 
 
 def test_large_magnitudes_stay_within_tolerance():
