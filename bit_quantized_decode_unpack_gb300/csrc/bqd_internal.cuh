@@ -36,7 +36,8 @@ int launch_qmv_generic(const QmvArgs &a, cudaStream_t s);
 // its shape/alignment envelope (the caller then uses the generic kernel).
 int launch_qmv_mma(const QmvArgs &a, cudaStream_t s);
 // Tensor-core decode path for 1/2-bit codes fed by a TMA shared-memory ring
-// (K a multiple of 256, 16-byte aligned rows); same contract.
+// (K a multiple of 256, K/gs a multiple of 8, 16-byte aligned rows and
+// bases); same contract.
 int launch_qmv_tma(const QmvArgs &a, cudaStream_t s);
 // Tensor-core decode path for t5 weights (K a multiple of 1024); same contract.
 int launch_qmv_t5(const QmvArgs &a, cudaStream_t s);

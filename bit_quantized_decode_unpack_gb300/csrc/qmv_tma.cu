@@ -37,6 +37,7 @@
 #include <stdio.h>
 #include <stdlib.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "bqd_internal.cuh"
@@ -51,10 +52,9 @@ __device__ unsigned int g_qmv_tma_timeouts = 0;
 
 constexpr int kCons = 8;                     // consumer warps
 constexpr int kThreadsT = (kCons + 1) * 32;  // + one producer warp
-constexpr int kRowsT = 16 * kCons;           // weight rows per CTA
 constexpr int kChunkT = 256;                 // codes per row per stage
 constexpr int kMaxStagesT = 8;
-constexpr int kMaxSplitT = 8;
+constexpr int kMaxSplitT = 16;  // cluster sizes above 8 are the non-portable ones
 constexpr size_t kSmemBudgetT = 112 * 1024;  // two CTAs per SM (with static smem and the 1 KB reserve)
 
 struct TmaParams {
@@ -63,8 +63,7 @@ struct TmaParams {
     const __half *biases;
     __half *out;
     float ratio;
-    int M, N, K, G, chunks, S, Cs, stages;
-    uint32_t ring_bytes;
+    int M, N, K, G, chunks, S, Cs, stages, RS, BX;
     uint32_t zero;  // always 0: keeps the magic constants opaque (in registers)
 };
 
@@ -91,23 +90,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
 }
-
-// cp.async of BYTES (4 or 8) bytes; src_bytes = 0 writes zeros and reads nothing
-template <int BYTES>
-__device__ __forceinline__ void cp_async(uint32_t dst, const void *src, uint32_t src_bytes)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(dst), "l"(src), "n"(BYTES), "r"(src_bytes)
-                 : "memory");
-}
-
-// arrive on `bar` once this thread's earlier cp.async copies have landed
-// (the barrier's expected count includes this arrival)
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCons * 32) : "memory"); }
 
 __device__ __forceinline__ void st_cluster_v2(uint32_t local_addr, uint32_t rank, float a, float b)
 {
@@ -296,30 +278,45 @@ __device__ __forceinline__ float h2f_hi(uint32_t w) { return __half2float(__usho
 
 // ---- the kernel --------------------------------------------------------------------
 
-template <int FMT, int GS>
-struct Layout {
-    static constexpr int kW = kRowsT * TF<FMT, GS>::kChunkBytes;  // weight tile bytes
-    static constexpr int kGPC = kChunkT / GS;                      // groups per chunk
-    static constexpr int kS = kRowsT * kGPC * 2;                   // scale (or bias) tile bytes
-    __host__ __device__ static constexpr int stage(bool bias) { return kW + kS * (bias ? 2 : 1); }
+constexpr int kRowsW = 32;              // weight rows per consumer warp: two MMA row tiles
+constexpr int kRowsC = kRowsW * kCons;   // weight rows per CTA
+
+// One ring stage = one 256-code chunk of the CTA's 256 rows:
+//   weights [256][CB] (TMA, swizzled) | B fragments [8][MP][4] uint4
+//   | Cx [4][8] f32 | Sx as fp16 (hi, lo) [8][4]
+// The scales and biases of the CTA's whole K range sit outside the ring, one
+// TMA box each: [256 rows][BX groups] fp16.
+template <int FMT, int GS, bool HAS_BIAS, int MP>
+struct Stage {
+    static constexpr int kGPC = kChunkT / GS;
+    static constexpr int kW = kRowsC * TF<FMT, GS>::kChunkBytes;
+    static constexpr int kB = kW;
+    static constexpr int kCx = kB + 8 * MP * 4 * 16;
+    static constexpr int kSx = kCx + 4 * 8 * 4;
+    static constexpr int kBytes = (kSx + 8 * 4 * 4 + 511) / 512 * 512;  // keeps the weight tile 512-aligned
 };
 
+constexpr int kXRawBytes = 8 * kChunkT * 2;  // producer's staging of one chunk of x (8 rows)
+
 template <int FMT, int GS, bool HAS_BIAS, int MP>
-__global__ void __launch_bounds__(kThreadsT, 2) qmv_tma_kernel(const __grid_constant__ CUtensorMap wmap, const TmaParams p)
+__global__ void __launch_bounds__(kThreadsT, 2)
+    qmv_tma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap,
+                   const __grid_constant__ CUtensorMap bmap, const TmaParams p)
 {
     using F = TF<FMT, GS>;
-    using L = Layout<FMT, GS>;
-    constexpr int GPC = L::kGPC;
+    using SL = Stage<FMT, GS, HAS_BIAS, MP>;
+    constexpr int GPC = SL::kGPC;
     constexpr int NPR = GS / 8;   // fp16x2 registers per (row, group)
     constexpr int MPG = GS / 16;  // MMAs per group
-    constexpr int STAGE = L::stage(HAS_BIAS);
+    constexpr uint32_t CB = F::kChunkBytes;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[kMaxStagesT], empty_bar[kMaxStagesT];
+    __shared__ __align__(8) uint64_t full_bar[kMaxStagesT], empty_bar[kMaxStagesT], sc_bar;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
     const int S = p.S;
     const int rank = S > 1 ? (int)cluster_ctarank() : 0;
-    const int n0 = (blockIdx.x / S) * kRowsT;
+    const int n0 = (blockIdx.x / S) * kRowsC;
     const int c_lo = rank * p.Cs;
     const int ncl = max(0, min(p.Cs, p.chunks - c_lo));
     const int NST = p.stages;
@@ -333,62 +330,168 @@ __global__ void __launch_bounds__(kThreadsT, 2) qmv_tma_kernel(const __grid_cons
     if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *ring = smem;
-    uint4 *Bs = reinterpret_cast<uint4 *>(smem + p.ring_bytes);            // [Cs][8][MP][4]
-    float *Cx = reinterpret_cast<float *>(Bs + (size_t)p.Cs * 8 * MP * 4);  // [Cs][4][8]
-    uint32_t *SxB = reinterpret_cast<uint32_t *>(Cx + (size_t)p.Cs * 32);  // [Cs][8][4]
-    float *red = reinterpret_cast<float *>(SxB + (size_t)p.Cs * 32);       // [S-1][128][8], rank 0's is used
+    const uint32_t ring_a = smem_addr(smem);
+    const uint32_t xraw_a = ring_a + (uint32_t)NST * SL::kBytes;  // [8][256] fp16
+    const uint32_t sc_a = xraw_a + kXRawBytes;                      // scales [256][BX] fp16
+    const uint32_t bi_a = sc_a + (uint32_t)(kRowsC * p.BX * 2);     // biases [256][BX] fp16
+    float *red = reinterpret_cast<float *>(smem + (size_t)NST * SL::kBytes + kXRawBytes +
+                                           (size_t)kRowsC * p.BX * 2 * (HAS_BIAS ? 2 : 1));  // [S][RS][8]
+    // the scale box starts at a 16-byte aligned group index
+    const int g0 = c_lo * GPC, gx = g0 & ~7;
 
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
-            mbar_init(smem_addr(&full_bar[s]), 33);  // producer lane 0 (expect_tx) + 32 cp.async arrivals
+            // producer lane 0 (expect_tx) + 32 arrivals once x is prepared
+            mbar_init(smem_addr(&full_bar[s]), 33);
             mbar_init(smem_addr(&empty_bar[s]), kCons * 32);
         }
+        mbar_init(smem_addr(&sc_bar), 1);
     }
     __syncthreads();
+    uint32_t mg[10];
+#pragma unroll
+    for (int i = 0; i < 10; ++i) mg[i] = F::magic_at(i < F::kNumMagic ? i : 0) ^ p.zero;
 
     if (warp == kCons) {
-        // ---- producer: weights by TMA, scales/biases by cp.async -----------------
-        // The first NST stages need no free slot and are requested at once (they
-        // do not depend on the previous kernel); later ones wait for a slot
-        // after griddepcontrol.wait, so no wait spins while an earlier kernel runs.
-        int issued = 0, s = 0;
+        // ---- producer ------------------------------------------------------------
+        // per stage: weights by TMA, scales/biases by cp.async, then x of the
+        // chunk turned into MMA B fragments, and Cx / Sx of its groups by the
+        // same MMA sequence as the consumers (row 0: all-zero codes, which
+        // unpack to exactly the magic values; row 1: ones).  With M <= 4,
+        // columns 4..7 of those MMAs carry a second group.
+        auto issue_weights = [&](int it, int s) {
+            if (lane == 0) {
+                const uint32_t bar = smem_addr(&full_bar[s]);
+                mbar_arrive_expect_tx(bar, (uint32_t)SL::kW);
+                tma_load_2d(ring_a + (uint32_t)s * SL::kBytes, &wmap, (c_lo + it) * (int)CB, n0, bar);
+            }
+        };
+        auto load_x = [&](int it, uint4 (&xv)[MP]) {
+#pragma unroll
+            for (int m = 0; m < MP; ++m) {
+                xv[m] = make_uint4(0, 0, 0, 0);
+                if (m < p.M) xv[m] = ld_x16(p.x + (size_t)m * p.K + (size_t)(c_lo + it) * kChunkT + 8 * lane);
+            }
+        };
+        uint32_t Az[NPR];
+        F::zero_group(mg, Az);
+        const uint32_t one2 = 0x3C003C00u;
+        // scales, biases and the weights of the first stages do not depend on
+        // the previous kernel
+        if (lane == 0 && ncl > 0) {
+            const uint32_t bx_bytes = (uint32_t)(kRowsC * p.BX * 2);
+            mbar_arrive_expect_tx(smem_addr(&sc_bar), bx_bytes * (HAS_BIAS ? 2 : 1));
+            tma_load_2d(sc_a, &smap, gx, n0, smem_addr(&sc_bar));
+            if (HAS_BIAS) tma_load_2d(bi_a, &bmap, gx, n0, smem_addr(&sc_bar));
+        }
+        const int pre = min(NST, ncl);
+        for (int it = 0; it < pre; ++it) issue_weights(it, it);
+        pdl_wait();
+        uint4 xv[MP];
+        if (ncl > 0) load_x(0, xv);
+        int s = 0, done = 0;
         uint32_t par = 0;
         for (int it = 0; it < ncl; ++it) {
-            if (it == NST) pdl_wait();
+            const uint32_t st = ring_a + (uint32_t)s * SL::kBytes;
             if (it >= NST) {
                 bool ok = lane == 0 ? wait_bounded(smem_addr(&empty_bar[s]), par ^ 1u) : true;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
+                issue_weights(it, s);
             }
-            const uint32_t bar = smem_addr(&full_bar[s]);
-            uint8_t *st = ring + (size_t)s * STAGE;
-            const int c = c_lo + it;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar, (uint32_t)L::kW);
-                tma_load_2d(smem_addr(st), &wmap, c * F::kChunkBytes, n0, bar);
-            }
+            // x of this chunk -> staging rows (zeros past M), then the next chunk's loads
 #pragma unroll
-            for (int i = 0; i < kRowsT / 32; ++i) {
-                const int r = lane + 32 * i;
-                const int n = n0 + r;
-                const bool ok = n < p.N;
-                const long long off = (long long)(ok ? n : 0) * p.G + (long long)c * GPC;
-                cp_async<GPC * 2>(smem_addr(st + L::kW + r * GPC * 2), p.scales + off, ok ? GPC * 2 : 0);
-                if (HAS_BIAS)
-                    cp_async<GPC * 2>(smem_addr(st + L::kW + L::kS + r * GPC * 2), p.biases + off, ok ? GPC * 2 : 0);
+            for (int m = 0; m < MP; ++m)
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(xraw_a + (uint32_t)(m * 512 + 16 * lane)),
+                             "r"(xv[m].x), "r"(xv[m].y), "r"(xv[m].z), "r"(xv[m].w)
+                             : "memory");
+            if (it + 1 < ncl) load_x(it + 1, xv);
+            __syncwarp();
+            // B fragments: 16 items per x row, each two 16-byte reads -> two entries
+#pragma unroll
+            for (int u = 0; u < MP / 2; ++u) {
+                const int e = lane + 32 * u;
+                const int i16 = e & 15, m = e >> 4;
+                int base, pp0, ts;
+                F::xitem(i16, base, pp0, ts);
+                const uint4 vl = lds128(xraw_a + (uint32_t)(m * 512 + base * 2));
+                const uint4 vh = lds128(xraw_a + (uint32_t)(m * 512 + (base + F::kHO) * 2));
+                const uint32_t d = st + SL::kB + (uint32_t)(((pp0 * MP + m) * 4 + ts) * 16);
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(d), "r"(__byte_perm(vl.x, vh.x, 0x5410)),
+                             "r"(__byte_perm(vl.x, vh.x, 0x7632)), "r"(__byte_perm(vl.y, vh.y, 0x5410)),
+                             "r"(__byte_perm(vl.y, vh.y, 0x7632))
+                             : "memory");
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(d + MP * 4 * 16),
+                             "r"(__byte_perm(vl.z, vh.z, 0x5410)), "r"(__byte_perm(vl.z, vh.z, 0x7632)),
+                             "r"(__byte_perm(vl.w, vh.w, 0x5410)), "r"(__byte_perm(vl.w, vh.w, 0x7632))
+                             : "memory");
             }
-            cp_async_arrive_noinc(bar);
-            issued = it + 1;
+            __syncwarp();
+            // Cx (row 0) and Sx (row 1) of the chunk's groups
+            {
+                constexpr int IPC = MP == 4 ? 2 : 1;
+                constexpr int NCH = GPC / IPC;
+                float d[NCH][4];
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) d[ch][0] = d[ch][1] = d[ch][2] = d[ch][3] = 0.f;
+#pragma unroll
+                for (int i = 0; i < MPG; i += 2) {
+                    const uint32_t a0 = g == 0 ? Az[2 * i] : (g == 1 ? one2 : 0u);
+                    const uint32_t a2 = g == 0 ? Az[2 * i + 1] : (g == 1 ? one2 : 0u);
+                    const uint32_t a0n = g == 0 ? Az[2 * i + 2] : (g == 1 ? one2 : 0u);
+                    const uint32_t a2n = g == 0 ? Az[2 * i + 3] : (g == 1 ? one2 : 0u);
+#pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        const int j = ch * IPC + ((IPC == 2 && g >= 4) ? 1 : 0);
+                        const int mi = j * MPG + i;
+                        const uint4 b = lds128(st + SL::kB + (uint32_t)((((mi >> 1) * MP + (g & (MP - 1))) * 4 + t) * 16));
+                        mma_k16(d[ch], a0, 0u, a2, 0u, b.x, b.y);
+                        mma_k16(d[ch], a0n, 0u, a2n, 0u, b.z, b.w);
+                    }
+                }
+                if (g < 2) {
+#pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        const int j = ch * IPC + ((IPC == 2 && t >= 2) ? 1 : 0);
+                        const int col0 = IPC == 2 ? 2 * (t & 1) : 2 * t;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const float v = d[ch][h];
+                            if (g == 0) {
+                                asm volatile("st.shared.f32 [%0], %1;" ::"r"(st + SL::kCx + (uint32_t)((j * 8 + col0 + h) * 4)),
+                                             "f"(v)
+                                             : "memory");
+                            } else {
+                                const __half vh = __float2half_rn(v);
+                                const __half vl = __float2half_rn(v - __half2float(vh));
+                                const uint32_t pk = (uint32_t)__half_as_ushort(vh) | ((uint32_t)__half_as_ushort(vl) << 16);
+                                const uint32_t sa = st + SL::kSx + (uint32_t)(((col0 + h) * 4 + j) * 4);
+                                asm volatile("st.shared.u32 [%0], %1;" ::"r"(sa), "r"(pk) : "memory");
+                                if (GPC == 2) asm volatile("st.shared.u32 [%0], %1;" ::"r"(sa + 8), "r"(0u) : "memory");
+                            }
+                        }
+                    }
+                }
+                // with M <= 4 the consumers' columns 4..7 repeat columns 0..3:
+                // their bias slots hold zeros
+                if (MP == 4 && lane < 16)
+                    asm volatile("st.shared.u32 [%0], %1;" ::"r"(st + SL::kSx + (uint32_t)((16 + lane) * 4)), "r"(0u)
+                                 : "memory");
+            }
+            mbar_arrive(smem_addr(&full_bar[s]));
+            done = it + 1;
             if (++s == NST) {
                 s = 0;
                 par ^= 1u;
             }
         }
-        // every copy this CTA issued has landed before anyone leaves
-        if (lane == 0)
-            for (int it = max(0, issued - NST); it < issued; ++it)
+        // every copy this CTA issued has landed before anyone leaves (each
+        // issued stage was also prepared, so its barrier can complete)
+        if (lane == 0) {
+            for (int it = max(0, done - NST); it < done; ++it)
                 wait_bounded(smem_addr(&full_bar[it % NST]), (it / NST) & 1);
+            if (ncl > 0) wait_bounded(smem_addr(&sc_bar), 0);
+        }
         __syncwarp();
         if (S > 1) {
             asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
@@ -397,180 +500,94 @@ __global__ void __launch_bounds__(kThreadsT, 2) qmv_tma_kernel(const __grid_cons
         return;
     }
 
-    // ---- consumers ---------------------------------------------------------------
-    const int g = lane >> 2, t = lane & 3;
-    pdl_wait();
-    // x -> B fragments: 16 items per (chunk, x row), four items per thread in
-    // flight, each two 16-byte loads filling two entries
-    {
-        const int items = ncl * MP * 16;
-        for (int e0 = tid; e0 < items; e0 += 4 * kCons * 32) {
-            uint4 vl[4], vh[4];
+    // ---- consumers: warp w owns rows 32w .. 32w+31 (two MMA row tiles) -------------
+    float acc[2][4], accb[2][4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int e = e0 + u * kCons * 32;
-                const int i16 = e & 15, m = (e >> 4) % MP, c = e / (16 * MP);
-                int base, pp0, ts;
-                F::xitem(i16, base, pp0, ts);
-                vl[u] = vh[u] = make_uint4(0, 0, 0, 0);
-                if (e < items && m < p.M) {
-                    const __half *xr = p.x + (size_t)m * p.K + (size_t)(c_lo + c) * kChunkT + base;
-                    vl[u] = ld_x16(xr);
-                    vh[u] = ld_x16(xr + F::kHO);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int e = e0 + u * kCons * 32;
-                if (e >= items) continue;
-                const int i16 = e & 15, m = (e >> 4) % MP, c = e / (16 * MP);
-                int base, pp0, ts;
-                F::xitem(i16, base, pp0, ts);
-                uint4 *d = Bs + (((size_t)c * 8 + pp0) * MP + m) * 4 + ts;
-                d[0] = make_uint4(__byte_perm(vl[u].x, vh[u].x, 0x5410), __byte_perm(vl[u].x, vh[u].x, 0x7632),
-                                  __byte_perm(vl[u].y, vh[u].y, 0x5410), __byte_perm(vl[u].y, vh[u].y, 0x7632));
-                d[MP * 4] = make_uint4(__byte_perm(vl[u].z, vh[u].z, 0x5410), __byte_perm(vl[u].z, vh[u].z, 0x7632),
-                                       __byte_perm(vl[u].w, vh[u].w, 0x5410), __byte_perm(vl[u].w, vh[u].w, 0x7632));
-            }
-        }
-    }
-    consumers_sync();
-    uint32_t mg[10];
-#pragma unroll
-    for (int i = 0; i < 10; ++i) mg[i] = F::magic_at(i < F::kNumMagic ? i : 0) ^ p.zero;
-    const uint32_t bs_a = smem_addr(Bs), cx_a = smem_addr(Cx), sx_a = smem_addr(SxB);
-    // Cx (the offsets' dot products, MMA row 0) and Sx (group sums, row 1) of
-    // each (chunk, group), by the same MMA sequence as the main loop: row 0 of
-    // A holds all-zero codes, i.e. exactly the magic values.  With M <= 4 the
-    // columns 4..7 carry a second (chunk, group).
-    {
-        constexpr int IPC = MP == 4 ? 2 : 1;
-        uint32_t Az[NPR];
-        F::zero_group(mg, Az);
-        const uint32_t one2 = 0x3C003C00u;
-        const int items = ncl * GPC;
-        for (int ch = warp; ch * IPC < items; ch += kCons) {
-            int it_l = ch * IPC + ((IPC == 2 && g >= 4) ? 1 : 0);
-            if (it_l >= items) it_l = ch * IPC;
-            const int c = it_l / GPC, j = it_l % GPC;
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint32_t bq = bs_a + (uint32_t)((((c * 8) * MP + (g & (MP - 1))) * 4 + t) * 16);
-#pragma unroll
-            for (int i = 0; i < MPG; i += 2) {
-                const int mi = j * MPG + i;
-                const uint4 b = lds128(bq + (uint32_t)((mi >> 1) * MP * 4 * 16));
-                const uint32_t a0 = g == 0 ? Az[2 * i] : (g == 1 ? one2 : 0u);
-                const uint32_t a2 = g == 0 ? Az[2 * i + 1] : (g == 1 ? one2 : 0u);
-                const uint32_t a0n = g == 0 ? Az[2 * i + 2] : (g == 1 ? one2 : 0u);
-                const uint32_t a2n = g == 0 ? Az[2 * i + 3] : (g == 1 ? one2 : 0u);
-                mma_k16(d, a0, 0u, a2, 0u, b.x, b.y);
-                mma_k16(d, a0n, 0u, a2n, 0u, b.z, b.w);
-            }
-            if (g < 2) {
-                // columns 2t, 2t+1 of this lane's row: item ch*IPC (+1 for t >= 2 when IPC == 2)
-                int it_c = ch * IPC + ((IPC == 2 && t >= 2) ? 1 : 0);
-                if (it_c < items) {
-                    const int cc = it_c / GPC, jj = it_c % GPC;
-                    const int col0 = IPC == 2 ? 2 * (t & 1) : 2 * t;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (g == 0) {
-                            Cx[((size_t)cc * 4 + jj) * 8 + col0 + h] = d[h];
-                        } else {
-                            const __half vh = __float2half_rn(d[h]);
-                            const __half vl = __float2half_rn(d[h] - __half2float(vh));
-                            SxB[((size_t)cc * 8 + col0 + h) * 4 + jj] =
-                                (uint32_t)__half_as_ushort(vh) | ((uint32_t)__half_as_ushort(vl) << 16);
-                            if (GPC == 2) SxB[((size_t)cc * 8 + col0 + h) * 4 + jj + 2] = 0u;
-                        }
-                    }
-                }
-            }
-        }
-        // with M <= 4 the main loop's columns 4..7 repeat columns 0..3: their
-        // bias slots must hold finite values (zeros)
-        if (MP == 4)
-            for (int i = tid; i < ncl * 4 * 4; i += kCons * 32) SxB[(size_t)(i >> 4) * 32 + 16 + (i & 15)] = 0u;
-    }
-    consumers_sync();
-
-    // ---- main loop: one chunk of the warp's 16 rows per stage ------------------
-    float acc[4] = {0.f, 0.f, 0.f, 0.f}, accb[4] = {0.f, 0.f, 0.f, 0.f};
-    const int r0 = warp * 16 + g;
-    const int jb = t & (GPC - 1);  // bias slot t: group t (gs=64), group t&1 for t < 2 (gs=128)
-    constexpr uint32_t R8W = 8 * F::kChunkBytes;  // row r0+8 in the weight tile
-    constexpr uint32_t R8S = 8 * GPC * 2;         // row r0+8 in the scale / bias tiles
+    for (int q = 0; q < 4; ++q) acc[0][q] = acc[1][q] = accb[0][q] = accb[1][q] = 0.f;
+    const int rb = warp * kRowsW + g;  // rows rb, rb+8 (tile 0), rb+16, rb+24 (tile 1)
+    const int jb = t & (GPC - 1);      // bias slot t: group t (gs=64), group t&1 for t < 2 (gs=128)
     uint32_t woff[F::kNW];
 #pragma unroll
-    for (int v = 0; v < F::kNW; ++v) woff[v] = F::word_off(r0, v, t);
-    const uint32_t soff = (uint32_t)(L::kW + r0 * GPC * 2);
-    const uint32_t boff = (uint32_t)(L::kW + L::kS + (r0 * GPC + jb) * 2);
-    uint32_t bq = bs_a + (uint32_t)((((g & (MP - 1)) * 4) + t) * 16);
-    uint32_t cq = cx_a + (uint32_t)(8 * t);
-    uint32_t sq = sx_a + (uint32_t)((g * 4 + t) * 4);
-    const uint32_t ring_a = smem_addr(ring);
+    for (int v = 0; v < F::kNW; ++v) woff[v] = F::word_off(rb, v, t);  // rows +8/16/24 share its swizzle
+    // scales / biases of row rb, group g0 - gx + GPC*it (+ jb for the bias slot)
+    const uint32_t R8S = (uint32_t)(8 * p.BX * 2);
+    uint32_t sq = sc_a + (uint32_t)((rb * p.BX + g0 - gx) * 2);
+    uint32_t bqb = bi_a + (uint32_t)((rb * p.BX + g0 - gx + jb) * 2);
+    const uint32_t bqo = (uint32_t)(SL::kB + (((g & (MP - 1)) * 4) + t) * 16);
+    const uint32_t cxo = (uint32_t)(SL::kCx + 8 * t);
+    const uint32_t sxo = (uint32_t)(SL::kSx + (g * 4 + t) * 4);
     uint32_t st_a = ring_a;
     int s = 0;
     uint32_t par = 0;
-    for (int it = 0; it < ncl; ++it) {
+    const bool sc_ok = ncl == 0 || wait_bounded(smem_addr(&sc_bar), 0);
+    for (int it = 0; it < ncl && sc_ok; ++it) {
         if (!wait_bounded(smem_addr(&full_bar[s]), par)) break;
-        uint32_t w0[F::kNW], w1[F::kNW];
+        uint32_t w[4][F::kNW];
 #pragma unroll
-        for (int v = 0; v < F::kNW; ++v) {
-            w0[v] = lds32(st_a + woff[v]);
-            w1[v] = lds32(st_a + woff[v] + R8W);
+        for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+            for (int v = 0; v < F::kNW; ++v) w[rr][v] = lds32(st_a + woff[v] + rr * 8 * CB);
+        // scales of the four rows for the chunk's groups
+        uint32_t sw[4][GPC / 2];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            if constexpr (GPC == 4) {
+                const uint2 a = lds64(sq + rr * R8S);
+                sw[rr][0] = a.x;
+                sw[rr][GPC / 2 - 1] = a.y;
+            } else {
+                sw[rr][0] = lds32(sq + rr * R8S);
+            }
         }
-        // scales of rows r0, r0+8 for the chunk's groups
-        uint32_t sw0[GPC / 2], sw1[GPC / 2];
-        if constexpr (GPC == 4) {
-            const uint2 a = lds64(st_a + soff), b = lds64(st_a + soff + R8S);
-            sw0[0] = a.x; sw0[GPC / 2 - 1] = a.y;
-            sw1[0] = b.x; sw1[GPC / 2 - 1] = b.y;
-        } else {
-            sw0[0] = lds32(st_a + soff);
-            sw1[0] = lds32(st_a + soff + R8S);
+        uint16_t bb[4];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            if constexpr (HAS_BIAS) {
+                bb[rr] = lds16(bqb + rr * R8S);
+            } else {
+                const uint32_t x0 = (jb >> 1) ? sw[rr][GPC / 2 - 1] : sw[rr][0];
+                bb[rr] = __half_as_ushort(sym_bias(__ushort_as_half((uint16_t)(x0 >> (16 * (jb & 1)))), p.ratio));
+            }
+            if (GPC == 2 && t >= 2) bb[rr] = 0;
         }
-        uint16_t b0, b1;
-        if constexpr (HAS_BIAS) {
-            b0 = lds16(st_a + boff);
-            b1 = lds16(st_a + boff + R8S);
-        } else {
-            const uint32_t x0 = (jb >> 1) ? sw0[GPC / 2 - 1] : sw0[0];
-            const uint32_t x1 = (jb >> 1) ? sw1[GPC / 2 - 1] : sw1[0];
-            b0 = __half_as_ushort(sym_bias(__ushort_as_half((uint16_t)(x0 >> (16 * (jb & 1)))), p.ratio));
-            b1 = __half_as_ushort(sym_bias(__ushort_as_half((uint16_t)(x1 >> (16 * (jb & 1)))), p.ratio));
-        }
-        if (GPC == 2 && t >= 2) b0 = b1 = 0;
-        // every read of the stage is issued above; release it once the values
-        // have arrived (the arrive orders after them)
+        const uint32_t bq = st_a + bqo;
 #pragma unroll
         for (int j = 0; j < GPC; ++j) {
-            uint32_t A0[NPR], A1[NPR];
-            F::unpack_group(w0, j, t, mg, A0);
-            F::unpack_group(w1, j, t, mg, A1);
-            float ag[4] = {0.f, 0.f, 0.f, 0.f};
+            float ag[2][4];
 #pragma unroll
-            for (int i = 0; i < MPG; i += 2) {
-                const int mi = j * MPG + i;
-                const uint4 b = lds128(bq + (uint32_t)((mi >> 1) * MP * 4 * 16));
-                mma_k16(ag, A0[2 * i], A1[2 * i], A0[2 * i + 1], A1[2 * i + 1], b.x, b.y);
-                mma_k16(ag, A0[2 * i + 2], A1[2 * i + 2], A0[2 * i + 3], A1[2 * i + 3], b.z, b.w);
+            for (int q = 0; q < 4; ++q) ag[0][q] = ag[1][q] = 0.f;
+#pragma unroll
+            for (int tl = 0; tl < 2; ++tl) {
+                uint32_t A0[NPR], A1[NPR];
+                F::unpack_group(w[2 * tl], j, t, mg, A0);
+                F::unpack_group(w[2 * tl + 1], j, t, mg, A1);
+#pragma unroll
+                for (int i = 0; i < MPG; i += 2) {
+                    const int mi = j * MPG + i;
+                    const uint4 b = lds128(bq + (uint32_t)((mi >> 1) * MP * 4 * 16));
+                    mma_k16(ag[tl], A0[2 * i], A1[2 * i], A0[2 * i + 1], A1[2 * i + 1], b.x, b.y);
+                    mma_k16(ag[tl], A0[2 * i + 2], A1[2 * i + 2], A0[2 * i + 3], A1[2 * i + 3], b.z, b.w);
+                }
             }
-            const uint2 cxv = lds64(cq + (uint32_t)(j * 32));
+            const uint2 cxv = lds64(st_a + cxo + (uint32_t)(j * 32));
             const float cx0 = __uint_as_float(cxv.x), cx1 = __uint_as_float(cxv.y);
-            const float sa = (j & 1) ? h2f_hi(sw0[j >> 1]) : h2f_lo(sw0[j >> 1]);
-            const float sb = (j & 1) ? h2f_hi(sw1[j >> 1]) : h2f_lo(sw1[j >> 1]);
-            acc[0] = fmaf(sa, ag[0] - cx0, acc[0]);
-            acc[1] = fmaf(sa, ag[1] - cx1, acc[1]);
-            acc[2] = fmaf(sb, ag[2] - cx0, acc[2]);
-            acc[3] = fmaf(sb, ag[3] - cx1, acc[3]);
+#pragma unroll
+            for (int tl = 0; tl < 2; ++tl) {
+                const float sa = (j & 1) ? h2f_hi(sw[2 * tl][j >> 1]) : h2f_lo(sw[2 * tl][j >> 1]);
+                const float sb = (j & 1) ? h2f_hi(sw[2 * tl + 1][j >> 1]) : h2f_lo(sw[2 * tl + 1][j >> 1]);
+                acc[tl][0] = fmaf(sa, ag[tl][0] - cx0, acc[tl][0]);
+                acc[tl][1] = fmaf(sa, ag[tl][1] - cx1, acc[tl][1]);
+                acc[tl][2] = fmaf(sb, ag[tl][2] - cx0, acc[tl][2]);
+                acc[tl][3] = fmaf(sb, ag[tl][3] - cx1, acc[tl][3]);
+            }
         }
-        mma_k8(accb, dup_half(b0), dup_half(b1), lds32(sq));
+        const uint32_t sxv = lds32(st_a + sxo);
+        mma_k8(accb[0], dup_half(bb[0]), dup_half(bb[1]), sxv);
+        mma_k8(accb[1], dup_half(bb[2]), dup_half(bb[3]), sxv);
         mbar_arrive(smem_addr(&empty_bar[s]));
-        bq += 8 * MP * 4 * 16;
-        cq += 128;
-        sq += 128;
-        st_a += STAGE;
+        sq += GPC * 2;
+        bqb += GPC * 2;
+        st_a += SL::kBytes;
         if (++s == NST) {
             s = 0;
             par ^= 1u;
@@ -578,37 +595,45 @@ __global__ void __launch_bounds__(kThreadsT, 2) qmv_tma_kernel(const __grid_cons
         }
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[q] += accb[q];
-    const int r1 = r0 + 8;
+    for (int q = 0; q < 4; ++q) {
+        acc[0][q] += accb[0][q];
+        acc[1][q] += accb[1][q];
+    }
 
     // ---- results -------------------------------------------------------------------
+    // value (tile tl, q) is row rb + 16 tl + 8 (q >> 1), column 2t + (q & 1)
     if (S == 1) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int n = n0 + (q < 2 ? r0 : r1), m = 2 * t + (q & 1);
-            if (n < p.N && m < p.M) p.out[(size_t)m * p.N + n] = __float2half_rn(acc[q]);
-        }
+        for (int tl = 0; tl < 2; ++tl)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int n = n0 + rb + 16 * tl + 8 * (q >> 1), m = 2 * t + (q & 1);
+                if (n < p.N && m < p.M) p.out[(size_t)m * p.N + n] = __float2half_rn(acc[tl][q]);
+            }
         return;
     }
-    // ranks 1..S-1 store their partials into rank 0's reduction area (not
-    // aliased with anything rank 0 may still be using), then one cluster
-    // barrier; rank 0 adds them in rank order
+    // reduce-scatter through distributed shared memory: rank q adds rows
+    // [q RS, (q+1) RS) of every rank's partials, in rank order
+    const int RS = p.RS;
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-    if (rank != 0) {
-        float *dst = red + (size_t)(rank - 1) * kRowsT * 8;
-        st_cluster_v2(smem_addr(dst + r0 * 8 + 2 * t), 0, acc[0], acc[1]);
-        st_cluster_v2(smem_addr(dst + r1 * 8 + 2 * t), 0, acc[2], acc[3]);
-    }
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    if (rank == 0) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int rr = q < 2 ? r0 : r1, m = 2 * t + (q & 1);
-            float v = acc[q];
-            for (int k = 1; k < S; ++k) v += red[((size_t)(k - 1) * kRowsT + rr) * 8 + m];
-            const int n = n0 + rr;
-            if (n < p.N && m < p.M) p.out[(size_t)m * p.N + n] = __float2half_rn(v);
+    for (int tl = 0; tl < 2; ++tl)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = rb + 16 * tl + 8 * h;
+            const int q = row / RS;
+            st_cluster_v2(smem_addr(red + ((size_t)rank * RS + (row - q * RS)) * 8 + 2 * t), (uint32_t)q,
+                          acc[tl][2 * h], acc[tl][2 * h + 1]);
         }
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    const int row0 = rank * RS;
+    const int nrow = min(RS, kRowsC - row0);
+    for (int e = tid; e < nrow * p.M; e += kCons * 32) {
+        const int lr = e / p.M, m = e % p.M;
+        float v = 0.f;
+        for (int k = 0; k < S; ++k) v += red[((size_t)k * RS + lr) * 8 + m];
+        const int n = n0 + row0 + lr;
+        if (n < p.N) p.out[(size_t)m * p.N + n] = __float2half_rn(v);
     }
 }
 
@@ -630,21 +655,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 struct TPlan {
-    int S, Cs, stages, R;
-    uint32_t ring;
+    int S, Cs, stages, R, RS, BX;
     size_t smem;
 };
 
-size_t tma_smem(int MP, int Cs, int S, uint32_t ring)
+template <int FMT, int GS, bool HAS_BIAS, int MP>
+size_t tma_smem(int S, int stages, int RS, int BX)
 {
-    return 1024 + ring + (size_t)Cs * (8 * MP * 4 * 16 + 32 * 4 + 32 * 4) + (size_t)(S - 1) * kRowsT * 8 * 4;
+    return 1024 + (size_t)stages * Stage<FMT, GS, HAS_BIAS, MP>::kBytes + kXRawBytes +
+           (size_t)kRowsC * BX * 2 * (HAS_BIAS ? 2 : 1) + (size_t)S * RS * 8 * 4;
 }
 
 template <int FMT, int GS, bool HAS_BIAS, int MP>
 int cluster_slots_t(int S, size_t smem)
 {
     struct Entry { int dev, S; size_t smem; int slots; };
-    static Entry cache[64];
+    static Entry cache[128];
     static int n = 0;
     static std::mutex mu;
     int dev = 0;
@@ -654,6 +680,7 @@ int cluster_slots_t(int S, size_t smem)
         if (cache[i].dev == dev && cache[i].S == S && cache[i].smem == smem) return cache[i].slots;
     auto kern = qmv_tma_kernel<FMT, GS, HAS_BIAS, MP>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudgetT);
+    cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S * 64);
     cfg.blockDim = dim3(kThreadsT);
@@ -670,43 +697,61 @@ int cluster_slots_t(int S, size_t smem)
         cudaGetLastError();
         slots = 0;
     }
-    if (n < 64) cache[n++] = Entry{dev, S, smem, slots};
+    if (n < 128) cache[n++] = Entry{dev, S, smem, slots};
     return slots;
 }
 
 template <int FMT, int GS, bool HAS_BIAS, int MP>
 bool plan_t(int N, int chunks, TPlan &best)
 {
-    const int R = (N + kRowsT - 1) / kRowsT;
+    constexpr int GPC = kChunkT / GS;
+    const int R = (N + kRowsC - 1) / kRowsC;
     const int sms = sm_count();
-    const uint32_t stage = (uint32_t)Layout<FMT, GS>::stage(HAS_BIAS);
+    const size_t stage = Stage<FMT, GS, HAS_BIAS, MP>::kBytes;
     double best_cost = 1e30;
     bool found = false;
     for (int S = 1; S <= kMaxSplitT && S <= chunks; ++S) {
         const int Cs = (chunks + S - 1) / S;
         if ((S - 1) * Cs >= chunks) continue;
-        // ring: as many stages as fit (at most Cs, at most kMaxStagesT)
-        const size_t fixed = tma_smem(MP, Cs, S, 0);
-        if (fixed + 2 * stage > kSmemBudgetT) continue;
+        const int RS = (kRowsC + S - 1) / S;
+        // scale box: the rank's groups from the 16-byte aligned group below its first
+        int maxoff = 0;
+        for (int r = 0; r < S; ++r) maxoff = std::max(maxoff, (r * Cs * GPC) & 7);
+        const int BX = (Cs * GPC + maxoff + 7) / 8 * 8;
+        if (BX > 256) continue;
+        const size_t fixed = tma_smem<FMT, GS, HAS_BIAS, MP>(S, 0, RS, BX);
+        if (fixed + stage > kSmemBudgetT) continue;
         int st = (int)((kSmemBudgetT - fixed) / stage);
         st = st > kMaxStagesT ? kMaxStagesT : st;
         st = st > Cs ? Cs : st;
-        if (st < 1) continue;
-        const uint32_t ring = (uint32_t)st * stage;
-        const size_t sm = tma_smem(MP, Cs, S, ring);
-        if (sm > kSmemBudgetT) continue;
+        if (st < 2 && Cs > 1) continue;
+        const size_t sm = tma_smem<FMT, GS, HAS_BIAS, MP>(S, st, RS, BX);
         const int slots = S == 1 ? 2 * sms : cluster_slots_t<FMT, GS, HAS_BIAS, MP>(S, sm);
         if (slots <= 0) continue;
         const int waves = (R + slots - 1) / slots;
-        // time ~ waves x (chunks per CTA + prologue/epilogue worth ~3 chunks)
-        const double cost = (double)waves * (Cs + 3) + 0.05 * S;
+        // time ~ waves x (chunks per CTA + first-stage latency and reduction, ~2 chunks)
+        const double cost = (double)waves * (Cs + 2) + 0.1 * S;
         if (cost < best_cost - 1e-9) {
             best_cost = cost;
-            best = TPlan{S, Cs, st, R, ring, sm};
+            best = TPlan{S, Cs, st, R, RS, BX, sm};
             found = true;
         }
     }
     return found;
+}
+
+// 2-D tensor map of a row-major [rows][cols] fp16 array, box {box_cols, 256}
+bool encode_f16(CUtensorMap &map, const __half *base, int64_t cols, int64_t rows, int box_cols)
+{
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)kRowsC};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int FMT, int GS, bool HAS_BIAS, int MP>
@@ -718,16 +763,22 @@ int launch_t(const TmaParams &p0, const CUtensorMap &map, int chunks, cudaStream
     p.S = pl.S;
     p.Cs = pl.Cs;
     p.stages = pl.stages;
-    p.ring_bytes = pl.ring;
+    p.RS = pl.RS;
+    p.BX = pl.BX;
+    CUtensorMap smap, bmap;
+    if (!encode_f16(smap, p.scales, p.G, p.N, pl.BX)) return BQD_ERR_CUDA;
+    bmap = smap;
+    if (HAS_BIAS && !encode_f16(bmap, p.biases, p.G, p.N, pl.BX)) return BQD_ERR_CUDA;
     if (getenv("BQD_DEBUG_PLAN"))
-        fprintf(stderr, "bqd tma plan: N=%d K=%d M=%d gs=%d -> S=%d Cs=%d stages=%d R=%d grid=%d smem=%zu\n", p.N, p.K,
-                p.M, GS, pl.S, pl.Cs, pl.stages, pl.R, pl.R * pl.S, pl.smem);
+        fprintf(stderr, "bqd tma plan: N=%d K=%d M=%d gs=%d -> S=%d Cs=%d stages=%d R=%d BX=%d grid=%d smem=%zu\n", p.N,
+                p.K, p.M, GS, pl.S, pl.Cs, pl.stages, pl.R, pl.BX, pl.R * pl.S, pl.smem);
     auto kern = qmv_tma_kernel<FMT, GS, HAS_BIAS, MP>;
     static int configured_dev[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured_dev[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudgetT) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudgetT) != cudaSuccess ||
+            cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
             return BQD_ERR_CUDA;
         configured_dev[dev] = 1;
     }
@@ -750,7 +801,7 @@ int launch_t(const TmaParams &p0, const CUtensorMap &map, int chunks, cudaStream
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, map, p) == cudaSuccess ? BQD_OK : BQD_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, kern, map, smap, bmap, p) == cudaSuccess ? BQD_OK : BQD_ERR_CUDA;
 }
 
 template <int FMT, int GS>
@@ -775,13 +826,11 @@ int take_qmv_tma_timeouts(unsigned int *count)
 int launch_qmv_tma(const QmvArgs &a, cudaStream_t s)
 {
     if (a.fmt != BQD_FMT_AFFINE1 && a.fmt != BQD_FMT_AFFINE2) return BQD_ERR_UNSUPPORTED;
-    // whole 256-code chunks; TMA needs 16-byte aligned rows and base; cp.async
-    // of a chunk's scales needs 4/8-byte alignment
-    if (a.K % kChunkT != 0 || a.row_bytes % 16 != 0) return BQD_ERR_UNSUPPORTED;
+    // whole 256-code chunks; the TMA boxes need 16-byte aligned bases and rows
+    // (weights: row_bytes, scales / biases: G fp16)
+    if (a.K % kChunkT != 0 || a.row_bytes % 16 != 0 || a.G % 8 != 0) return BQD_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(a.w) & 15) || (reinterpret_cast<uintptr_t>(a.x) & 15)) return BQD_ERR_UNSUPPORTED;
-    const uintptr_t salign = (uintptr_t)(kChunkT / a.gs) * 2;
-    if ((reinterpret_cast<uintptr_t>(a.scales) & (salign - 1)) ||
-        (a.biases && (reinterpret_cast<uintptr_t>(a.biases) & (salign - 1))))
+    if ((reinterpret_cast<uintptr_t>(a.scales) & 15) || (a.biases && (reinterpret_cast<uintptr_t>(a.biases) & 15)))
         return BQD_ERR_UNSUPPORTED;
     if (a.K > (int64_t)1 << 28 || a.N > (int64_t)1 << 28) return BQD_ERR_UNSUPPORTED;
     auto enc = encode_fn();
@@ -791,7 +840,7 @@ int launch_qmv_tma(const QmvArgs &a, cudaStream_t s)
     CUtensorMap map;
     cuuint64_t dims[2] = {(cuuint64_t)a.row_bytes, (cuuint64_t)a.N};
     cuuint64_t strides[1] = {(cuuint64_t)a.row_bytes};
-    cuuint32_t box[2] = {b64 ? 64u : 32u, (cuuint32_t)kRowsT};
+    cuuint32_t box[2] = {b64 ? 64u : 32u, (cuuint32_t)kRowsC};
     cuuint32_t estr[2] = {1, 1};
     CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.w), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, b64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
@@ -803,8 +852,7 @@ int launch_qmv_tma(const QmvArgs &a, cudaStream_t s)
     p.N = (int)a.N; p.K = (int)a.K; p.G = (int)a.G;
     p.chunks = (int)(a.K / kChunkT);
     p.zero = 0;
-    p.S = p.Cs = p.stages = 0;
-    p.ring_bytes = 0;
+    p.S = p.Cs = p.stages = p.RS = 0;
     const bool hb = a.biases != nullptr;
     for (int64_t m0 = 0; m0 < a.M; m0 += 8) {
         const int M = (int)((a.M - m0) < 8 ? (a.M - m0) : 8);

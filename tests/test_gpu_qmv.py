@@ -76,19 +76,33 @@ def test_tensor_core_paths_forced(kernel, fmt, gs, sym):
         run_case(p, kernel)
 
 
-# TMA-ring kernel: one 256-code chunk, row blocks of 128 with ragged tails,
-# split-K clusters of several sizes, M up to 8 and two passes for M > 8
-TMA_SHAPES = [(1, 1, 256), (2, 127, 256), (3, 128, 512), (4, 129, 768), (5, 383, 4096), (7, 1024, 5120),
-              (8, 2000, 1280), (9, 200, 2304), (16, 130, 1024), (1, 5120, 17408), (5, 300, 17408)]
+# TMA-ring kernel: its envelope is K a multiple of 256 with K/gs a multiple of
+# 8 (16-byte scale rows); shapes span row blocks of 256 with ragged tails,
+# split-K clusters of many sizes (portable and not), M up to 8 and two passes
+# for M > 8
+TMA_SHAPES = [(1, 1, 1024), (2, 127, 1024), (3, 256, 2048), (4, 257, 3072), (5, 383, 4096), (7, 1024, 5120),
+              (8, 2000, 1024), (9, 200, 2048), (16, 130, 1024), (1, 5120, 17408), (5, 300, 17408), (2, 4096, 6144)]
 
 
 @pytest.mark.parametrize("fmt", [F1, F2])
 @pytest.mark.parametrize("gs", [64, 128])
 @pytest.mark.parametrize("sym", [False, True])
 def test_tma_kernel_shapes(fmt, gs, sym):
-    for M, N, K in TMA_SHAPES:
+    shapes = TMA_SHAPES + ([(3, 257, 512), (1, 40, 512)] if gs == 64 else [])
+    for M, N, K in shapes:
         p = synth.problem(fmt, M, N, K, gs, sym=sym)
         run_case(p, "tma")
+
+
+@pytest.mark.parametrize("fmt", [F1, F2])
+def test_tma_envelope_and_fallback(fmt):
+    """Outside the TMA kernel's envelope (here K/gs = 12 groups) a forced call
+    reports "unsupported" and the default dispatch still gives parity."""
+    p = synth.problem(fmt, 3, 100, 768, 64)
+    with pytest.raises(bqd.BqdError) as ei:
+        run_case(p, "tma")
+    assert ei.value.status == 2  # BQD_ERR_UNSUPPORTED
+    run_case(p, None)
 
 
 @pytest.mark.parametrize("kernel", ["tma", "mma", "generic"])
