@@ -26,8 +26,8 @@ int sm_count()
 // Testing override of the dispatcher: BQD_FORCE_KERNEL=generic|mma|tma (read
 // on every call so that a test can compare the kernels in one process).
 // "mma" forces the register-streaming tensor-core kernels, "tma" the
-// TMA-ring kernel for 1/2-bit codes; a forced kernel's "unsupported" is
-// returned as is.
+// TMA-ring kernels (1/2-bit and t5 decode); a forced kernel's "unsupported"
+// is returned as is.
 static int forced_kernel()
 {
     const char *v = getenv("BQD_FORCE_KERNEL");
@@ -108,9 +108,10 @@ static int qmv_common(const void *x, const void *w, const void *scales, const vo
             int st = launch_qmm_t5(a, s);
             if (st != BQD_ERR_UNSUPPORTED || force == 2) return st;
         }
-        if (format != BQD_FMT_T5 && force != 2) {
-            // 1/2-bit: TMA-ring kernel (K a multiple of 256, aligned rows)
-            int st = launch_qmv_tma(a, s);
+        if (force != 2) {
+            // TMA-ring kernels (1/2-bit: K a multiple of 256; t5: of 1024;
+            // aligned rows and bases)
+            int st = format == BQD_FMT_T5 ? launch_qmv_t5r(a, s) : launch_qmv_tma(a, s);
             if (st != BQD_ERR_UNSUPPORTED || force == 3) return st;
         }
         int st = format == BQD_FMT_T5 ? launch_qmv_t5(a, s) : launch_qmv_mma(a, s);
@@ -206,7 +207,7 @@ extern "C" int bqd_detect_sym(const void *scales, const void *biases, int64_t N,
 extern "C" int bqd_device_status(bqd_stream_t stream)
 {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return BQD_ERR_CUDA;
-    unsigned int n1 = 0, n2 = 0, n3 = 0, n4 = 0;
+    unsigned int n1 = 0, n2 = 0, n3 = 0, n4 = 0, n5 = 0;
     int st = take_qmv_mma_timeouts(&n1);
     if (st != BQD_OK) return st;
     st = take_qmv_t5_timeouts(&n2);
@@ -215,5 +216,7 @@ extern "C" int bqd_device_status(bqd_stream_t stream)
     if (st != BQD_OK) return st;
     st = take_qmv_tma_timeouts(&n4);
     if (st != BQD_OK) return st;
-    return (n1 || n2 || n3 || n4) ? BQD_ERR_TIMEOUT : BQD_OK;
+    st = take_qmv_t5r_timeouts(&n5);
+    if (st != BQD_OK) return st;
+    return (n1 || n2 || n3 || n4 || n5) ? BQD_ERR_TIMEOUT : BQD_OK;
 }

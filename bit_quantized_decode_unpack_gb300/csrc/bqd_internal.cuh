@@ -39,6 +39,9 @@ int launch_qmv_mma(const QmvArgs &a, cudaStream_t s);
 // (K a multiple of 256, K/gs a multiple of 8, 16-byte aligned rows and
 // bases); same contract.
 int launch_qmv_tma(const QmvArgs &a, cudaStream_t s);
+// Tensor-core decode path for t5 weights fed by a TMA shared-memory ring (K a
+// multiple of 1024, K/gs a multiple of 8, 16-byte aligned bases); same contract.
+int launch_qmv_t5r(const QmvArgs &a, cudaStream_t s);
 // Tensor-core decode path for t5 weights (K a multiple of 1024); same contract.
 int launch_qmv_t5(const QmvArgs &a, cudaStream_t s);
 // t5 prefill matrix product on tcgen05 tensor cores (meant for M > 16).
@@ -69,6 +72,7 @@ int take_qmv_mma_timeouts(unsigned int *count);
 int take_qmv_t5_timeouts(unsigned int *count);
 int take_qmm_timeouts(unsigned int *count);
 int take_qmv_tma_timeouts(unsigned int *count);
+int take_qmv_t5r_timeouts(unsigned int *count);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

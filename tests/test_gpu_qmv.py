@@ -63,7 +63,7 @@ MMA_SHAPES = [(1, 17, 1024), (2, 300, 2048), (3, 130, 3072), (5, 1000, 1024), (8
               (4, 16, 5120), (6, 1, 1024)]
 
 
-@pytest.mark.parametrize("kernel,fmt", [("mma", F1), ("mma", F2), ("mma", T5), ("tma", F1), ("tma", F2)])
+@pytest.mark.parametrize("kernel,fmt", [("mma", F1), ("mma", F2), ("mma", T5), ("tma", F1), ("tma", F2), ("tma", T5)])
 @pytest.mark.parametrize("gs", [64, 128])
 @pytest.mark.parametrize("sym", [False, True])
 def test_tensor_core_paths_forced(kernel, fmt, gs, sym):
@@ -91,6 +91,22 @@ def test_tma_kernel_shapes(fmt, gs, sym):
     shapes = TMA_SHAPES + ([(3, 257, 512), (1, 40, 512)] if gs == 64 else [])
     for M, N, K in shapes:
         p = synth.problem(fmt, M, N, K, gs, sym=sym)
+        run_case(p, "tma")
+
+
+# t5 TMA-ring kernel: K a multiple of 1024; ragged 128-row blocks, split-K
+# clusters, passes of at most 6 x rows (M = 7, 12, 16 take several)
+T5R_SHAPES = [(1, 1, 1024), (2, 127, 1024), (3, 129, 2048), (4, 300, 3072), (5, 1000, 5120), (6, 383, 4096),
+              (7, 260, 2048), (12, 64, 1024), (16, 130, 2048), (1, 5120, 17408), (5, 200, 17408)]
+
+
+@pytest.mark.parametrize("gs", [64, 128])
+@pytest.mark.parametrize("sym", [False, True])
+def test_t5_tma_kernel_shapes(gs, sym):
+    for M, N, K in T5R_SHAPES:
+        p = synth.problem(T5, M, N, K, gs, sym=sym)
+        if not sym:
+            p["biases"] = synth.biases(np.random.default_rng(N + M), F2, p["scales"])
         run_case(p, "tma")
 
 
@@ -272,8 +288,7 @@ def test_large_scales_take_the_exact_unpack(fmt):
     p["x"] = (p["x"].astype(np.float32) * 1e-3).astype(np.float16)
     run_case(p, "mma")
     run_case(p, None)
-    if fmt != T5:
-        run_case(p, "tma")
+    run_case(p, "tma")
 
 
 def test_large_magnitudes_stay_within_tolerance():
