@@ -501,9 +501,9 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     }
 
     // ---- consumers: warp w owns rows 32w .. 32w+31 (two MMA row tiles) -------------
-    float acc[2][4], accb[2][4];
+    float acc[2][4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[0][q] = acc[1][q] = accb[0][q] = accb[1][q] = 0.f;
+    for (int q = 0; q < 4; ++q) acc[0][q] = acc[1][q] = 0.f;
     const int rb = warp * kRowsW + g;  // rows rb, rb+8 (tile 0), rb+16, rb+24 (tile 1)
     const int jb = t & (GPC - 1);      // bias slot t: group t (gs=64), group t&1 for t < 2 (gs=128)
     uint32_t woff[F::kNW];
@@ -516,17 +516,14 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     const uint32_t bqo = (uint32_t)(SL::kB + (((g & (MP - 1)) * 4) + t) * 16);
     const uint32_t cxo = (uint32_t)(SL::kCx + 8 * t);
     const uint32_t sxo = (uint32_t)(SL::kSx + (g * 4 + t) * 4);
+    // words of group j that a thread unpacks (per row): GS/64 for 2-bit, one for 1-bit
+    constexpr int WPG = FMT == BQD_FMT_AFFINE2 ? GS / 64 : 1;
     uint32_t st_a = ring_a;
     int s = 0;
     uint32_t par = 0;
     const bool sc_ok = ncl == 0 || wait_bounded(smem_addr(&sc_bar), 0);
     for (int it = 0; it < ncl && sc_ok; ++it) {
         if (!wait_bounded(smem_addr(&full_bar[s]), par)) break;
-        uint32_t w[4][F::kNW];
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr)
-#pragma unroll
-            for (int v = 0; v < F::kNW; ++v) w[rr][v] = lds32(st_a + woff[v] + rr * 8 * CB);
         // scales of the four rows for the chunk's groups
         uint32_t sw[4][GPC / 2];
 #pragma unroll
@@ -539,20 +536,35 @@ __global__ void __launch_bounds__(kThreadsT, 2)
                 sw[rr][0] = lds32(sq + rr * R8S);
             }
         }
-        uint16_t bb[4];
+        // bias term first, straight into the accumulators
+        {
+            uint16_t bb[4];
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-            if constexpr (HAS_BIAS) {
-                bb[rr] = lds16(bqb + rr * R8S);
-            } else {
-                const uint32_t x0 = (jb >> 1) ? sw[rr][GPC / 2 - 1] : sw[rr][0];
-                bb[rr] = __half_as_ushort(sym_bias(__ushort_as_half((uint16_t)(x0 >> (16 * (jb & 1)))), p.ratio));
+            for (int rr = 0; rr < 4; ++rr) {
+                if constexpr (HAS_BIAS) {
+                    bb[rr] = lds16(bqb + rr * R8S);
+                } else {
+                    const uint32_t x0 = (jb >> 1) ? sw[rr][GPC / 2 - 1] : sw[rr][0];
+                    bb[rr] = __half_as_ushort(sym_bias(__ushort_as_half((uint16_t)(x0 >> (16 * (jb & 1)))), p.ratio));
+                }
+                if (GPC == 2 && t >= 2) bb[rr] = 0;
             }
-            if (GPC == 2 && t >= 2) bb[rr] = 0;
+            const uint32_t sxv = lds32(st_a + sxo);
+            mma_k8(acc[0], dup_half(bb[0]), dup_half(bb[1]), sxv);
+            mma_k8(acc[1], dup_half(bb[2]), dup_half(bb[3]), sxv);
         }
         const uint32_t bq = st_a + bqo;
 #pragma unroll
         for (int j = 0; j < GPC; ++j) {
+            // this group's words of the four rows, read when needed
+            uint32_t w[4][F::kNW];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                for (int v = 0; v < WPG; ++v) {
+                    const int idx = j * WPG + v;
+                    w[rr][idx] = lds32(st_a + woff[idx] + rr * 8 * CB);
+                }
             float ag[2][4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) ag[0][q] = ag[1][q] = 0.f;
@@ -581,9 +593,6 @@ __global__ void __launch_bounds__(kThreadsT, 2)
                 acc[tl][3] = fmaf(sb, ag[tl][3] - cx1, acc[tl][3]);
             }
         }
-        const uint32_t sxv = lds32(st_a + sxo);
-        mma_k8(accb[0], dup_half(bb[0]), dup_half(bb[1]), sxv);
-        mma_k8(accb[1], dup_half(bb[2]), dup_half(bb[3]), sxv);
         mbar_arrive(smem_addr(&empty_bar[s]));
         sq += GPC * 2;
         bqb += GPC * 2;
@@ -593,11 +602,6 @@ __global__ void __launch_bounds__(kThreadsT, 2)
             par ^= 1u;
             st_a = ring_a;
         }
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        acc[0][q] += accb[0][q];
-        acc[1][q] += accb[1][q];
     }
 
     // ---- results -------------------------------------------------------------------
