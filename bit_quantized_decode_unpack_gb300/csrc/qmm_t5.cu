@@ -7,23 +7,26 @@
 //   Y[m, n] = sum_k X[m, k] * W[n, k],  W[n, k] = fp16(s[n,g] * t[n,k] + b[n,g])
 //   (sym: b = fp16(-ratio * s), default ratio 1 -> W = s*(t-1), exact in fp16)
 //
-// One CTA owns 128 weight rows x BX activation rows (BX = 32, 64 or 128) and a
-// range of K groups.  When the (weight, activation) tiles are too few to fill
-// the GPU, the K range is split over the CTAs of a cluster and the partial
-// tiles are reduced through distributed shared memory (no global scratch).
+// One CTA owns 128 weight rows x BX activation rows (BX = 32, 64, 128 or 256)
+// and a range of K groups.  When the (weight, activation) tiles are too few to
+// fill the GPU, the K range is split over the CTAs of a cluster and the
+// partial tiles are reduced through distributed shared memory (no global
+// scratch).
 //
-// Roles (192 threads):
-//   warps 0-3  decode: thread r owns weight row n0+r.  Per K step (one group
-//              of gs codes) it loads the row's t5 bytes, decodes them with a
-//              shared byte->trits table, forms the fp16 weights (magic-exponent
-//              LOP3 + HFMA2 gives s*t exactly, then + b) and stores them into
-//              the stage's A tile in the tcgen05 K-major 128-byte-swizzled
-//              layout.  After the K loop the same warps drain the TMEM
-//              accumulator (tcgen05.ld) and store Y.
-//   warp 4     allocates TMEM; lane 0 issues tcgen05.mma (kind::f16, M=128,
+// Roles (320 threads):
+//   warps 0-7  decode: thread (r, h) = (tid % 128, warp / 4) decodes half h of
+//              weight row n0+r's group per K step (one group of gs codes):
+//              codes [0, gs/2) or [gs/2, gs), both starting on an even byte,
+//              so byte pairs decode as a unit.  It loads the group's t5 bytes,
+//              decodes them with a shared byte->trits table, forms the fp16
+//              weights (magic-exponent LOP3 + HFMA2 gives s*t exactly, then
+//              + b) and stores them into the stage's A tile in the tcgen05
+//              K-major 128-byte-swizzled layout.  After the K loop warp w
+//              drains TMEM lanes 32(w%4)..+31, columns of half w/4, and stores Y.
+//   warp 8     allocates TMEM; lane 0 issues tcgen05.mma (kind::f16, M=128,
 //              N=BX, K=16, fp32 accumulation in TMEM) and tcgen05.commit, which
 //              frees a stage once its MMAs have completed.
-//   warp 5     lane 0 loads X tiles with TMA (cp.async.bulk.tensor, 128-byte
+//   warp 9     lane 0 loads X tiles with TMA (cp.async.bulk.tensor, 128-byte
 //              swizzle, zero fill past M).
 // Every mbarrier wait is bounded; on expiry the CTA stops issuing work, drains
 // what it issued (bounded), passes its remaining barriers and frees TMEM; the
@@ -42,7 +45,11 @@ namespace {
 
 using namespace qmvdev;
 
-constexpr int kThreadsQ = 192;
+constexpr int kDecodeWarpsQ = 8;                       // decode + epilogue warps
+constexpr int kDecodeThreadsQ = kDecodeWarpsQ * 32;
+constexpr int kMmaWarpQ = kDecodeWarpsQ;                // TMEM owner, MMA issuer
+constexpr int kTmaWarpQ = kDecodeWarpsQ + 1;            // x tiles by TMA
+constexpr int kThreadsQ = (kDecodeWarpsQ + 2) * 32;
 constexpr int kMaxStagesQ = 8;
 constexpr size_t kQmmSmemMax = 220 * 1024;
 
@@ -208,13 +215,13 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(smem_addr(&x_full[s]), 1);
-            mbar_init(smem_addr(&a_full[s]), 128);
+            mbar_init(smem_addr(&a_full[s]), kDecodeThreadsQ);
             mbar_init(smem_addr(&empty_bar[s]), 1);
         }
         mbar_init(smem_addr(&done_bar), 1);
         abort_flag = 0;
     }
-    if (warp == 4) tmem_alloc(smem_addr(&tmem_base), (uint32_t)p.bx);
+    if (warp == kMmaWarpQ) tmem_alloc(smem_addr(&tmem_base), (uint32_t)p.bx);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -222,7 +229,7 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
 
     pdl_wait();
 
-    if (warp == 5) {
+    if (warp == kTmaWarpQ) {
         // ---- X producer ---------------------------------------------------------
         if (lane == 0) {
             int issued = 0;
@@ -246,7 +253,7 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
                     wait_bounded(smem_addr(&x_full[it % NST]), (it / NST) & 1);
             }
         }
-    } else if (warp == 4) {
+    } else if (warp == kMmaWarpQ) {
         // ---- MMA issuer -----------------------------------------------------------
         if (lane == 0) {
             const uint32_t idesc = idesc_f16(128, p.bx);
@@ -272,8 +279,10 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
             tc_commit(smem_addr(&done_bar));  // arrives once every issued MMA has completed
         }
     } else {
-        // ---- decode warps: weight row n0 + tid ---------------------------------------
-        const int r = tid;
+        // ---- decode warps: weight row n0 + (tid & 127); warps 0-3 decode codes
+        // [0, GS/2) of each group, warps 4-7 codes [GS/2, GS) (warp-uniform) -----
+        const int r = tid & 127;
+        const int h = warp >> 2;
         const int row = n0 + r;
         const bool rok = row < p.N;
         const uint8_t *wrow = p.w + (long long)(rok ? row : 0) * p.row_bytes;
@@ -282,32 +291,40 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
         uint32_t mg[5];
 #pragma unroll
         for (int d = 0; d < 5; ++d) mg[d] = magic(2 * d) ^ p.zero;
+        // the group's bytes (aligned 32-bit loads, realigned with funnel shifts;
+        // row_bytes is a multiple of 16 here), scale and bias: the next K step's
+        // are requested before this one is decoded
+        constexpr int NW = (B + 3 + 3) / 4;
+        // the group's bytes (aligned 32-bit loads, realigned with funnel shifts;
+        // row_bytes is a multiple of 16 here), scale and bias: the next K step's
+        // are requested before this one is decoded
+        uint32_t raw_n[NW + 1];
+        int sh_n = 0;
+        uint16_t sb_n = 0, bb_n = 0;
+        auto fetch = [&](int g) {
+            const long long off = (long long)g * B;
+            const long long aoff = off & ~3LL;
+            const uint32_t *base = reinterpret_cast<const uint32_t *>(wrow + aoff);
+            sh_n = (int)(off & 3) * 8;
+#pragma unroll
+            for (int q = 0; q <= NW; ++q) raw_n[q] = (rok && aoff + 4 * q < p.row_bytes) ? base[q] : 0u;
+            sb_n = rok ? __half_as_ushort(srow[g]) : (uint16_t)0;
+            bb_n = rok && brow ? __half_as_ushort(brow[g]) : (uint16_t)0;
+        };
+        if (steps > 0) fetch(g_lo);
         for (int it = 0; it < steps; ++it) {
             const int s = it % NST;
+            uint32_t bytes_w[NW];
+#pragma unroll
+            for (int q = 0; q < NW; ++q) bytes_w[q] = __funnelshift_r(raw_n[q], raw_n[q + 1], sh_n);
+            const uint16_t sb = sb_n;
+            const uint16_t bb = rok ? (brow ? bb_n : __half_as_ushort(sym_bias(__ushort_as_half(sb), p.ratio)))
+                                    : (uint16_t)0;
+            if (it + 1 < steps) fetch(g_lo + it + 1);
             if (it >= NST && !wait_bounded(smem_addr(&empty_bar[s]), ((it / NST) - 1) & 1)) {
                 abort_flag = 1;
                 break;
             }
-            const int g = g_lo + it;
-            // the group's bytes, via aligned 32-bit loads realigned with funnel
-            // shifts (row_bytes is a multiple of 16 here)
-            constexpr int NW = (B + 3 + 3) / 4;
-            uint32_t bytes_w[NW];
-            {
-                const long long off = (long long)g * B;
-                const long long aoff = off & ~3LL;
-                const uint32_t *base = reinterpret_cast<const uint32_t *>(wrow + aoff);
-                const int sh = (int)(off & 3) * 8;
-                uint32_t raw[NW + 1];
-#pragma unroll
-                for (int q = 0; q <= NW; ++q) raw[q] = (rok && aoff + 4 * q < p.row_bytes) ? base[q] : 0u;
-#pragma unroll
-                for (int q = 0; q < NW; ++q) bytes_w[q] = __funnelshift_r(raw[q], raw[q + 1], sh);
-            }
-            const uint16_t sb = rok ? __half_as_ushort(srow[g]) : (uint16_t)0;
-            const uint16_t bb = rok ? (brow ? __half_as_ushort(brow[g])
-                                            : __half_as_ushort(sym_bias(__ushort_as_half(sb), p.ratio)))
-                                    : (uint16_t)0;
             const uint32_t s2 = dup_half(sb), b2 = dup_half(bb);
             // constants -2^(10-2d)*s stay finite for |s| < 63; else the exact
             // (magic - offset) * s form is used
@@ -317,36 +334,67 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
             for (int d = 0; d < 5; ++d)
                 c[d] = hmul2(s2, dup_half(__half_as_ushort(__float2half_rn(-(float)(1024 >> (2 * d))))));
             auto wv = [&](uint32_t field_word, uint32_t mask, int d) -> uint32_t {
-                const uint32_t h = (field_word & mask) | mg[d];
-                const uint32_t ts = fast ? hfma2(h, s2, c[d]) : hmul2(hsub2(h, mg[d]), s2);  // t*s, exact
+                const uint32_t hh = (field_word & mask) | mg[d];
+                const uint32_t ts = fast ? hfma2(hh, s2, c[d]) : hmul2(hsub2(hh, mg[d]), s2);  // t*s, exact
                 return hadd2(ts, b2);
             };
             auto lut_of = [&](int j) -> uint32_t { return lut[__byte_perm(bytes_w[j >> 2], 0, 0x4440 | (j & 3))]; };
-            // codes of the group in order, two per 32-bit word (code 2i low, 2i+1 high)
-            uint32_t hv[GS / 2];
-#pragma unroll
-            for (int j = 0; j + 1 < B; j += 2) {
+            // codes 5j .. 5j+9 of bytes (j, j+1), two per 32-bit word (code 2i low, 2i+1 high)
+            auto pair_at = [&](int j, uint32_t *out) {
                 const uint32_t L0 = lut_of(j), L1 = lut_of(j + 1);
                 const uint32_t u = L0 * 16385u;      // fields of byte j, also shifted by 14
                 const uint32_t u2 = L0 + (L1 << 24);  // (trit 4 of byte j, trit 0 of byte j+1) at bit 8
                 const uint32_t u3 = L1 * 16385u;     // fields of byte j+1, also shifted by 14
-                const int k = 5 * j;                 // first code of byte j (even)
-                hv[k / 2] = wv(u, 0x00030003u, 0);
-                hv[k / 2 + 1] = wv(u, 0x00300030u, 2);
-                hv[k / 2 + 2] = wv(u2, 0x03000300u, 4);
-                if (k / 2 + 3 < GS / 2) hv[k / 2 + 3] = wv(u3, 0x000C000Cu, 1);
-                if (k / 2 + 4 < GS / 2) hv[k / 2 + 4] = wv(u3, 0x00C000C0u, 3);
+                out[0] = wv(u, 0x00030003u, 0);
+                out[1] = wv(u, 0x00300030u, 2);
+                out[2] = wv(u2, 0x03000300u, 4);
+                out[3] = wv(u3, 0x000C000Cu, 1);
+                out[4] = wv(u3, 0x00C000C0u, 3);
+            };
+            // codes 5j .. 5j+3 of a lone byte j
+            auto single_at = [&](int j, uint32_t *out) {
+                const uint32_t u = lut_of(j) * 16385u;
+                out[0] = wv(u, 0x00030003u, 0);
+                out[1] = wv(u, 0x00300030u, 2);
+            };
+            // this thread's GS/4 words (GS/2 codes): half h of the group
+            uint32_t hv[GS / 4];
+            if (GS == 128) {
+                if (h == 0) {  // codes 0..63: byte pairs (0,1) .. (10,11), then byte 12's first four
+#pragma unroll
+                    for (int jp = 0; jp < 6; ++jp) pair_at(2 * jp, &hv[5 * jp]);
+                    single_at(12, &hv[30]);
+                } else {  // codes 64..127: byte pairs (12,13) .. (24,25) give codes 60..129
+                    uint32_t tmp[35];
+#pragma unroll
+                    for (int jp = 0; jp < 7; ++jp) pair_at(12 + 2 * jp, &tmp[5 * jp]);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) hv[i] = tmp[i + 2];
+                }
+            } else {
+                if (h == 0) {  // codes 0..31: byte pairs (0,1) .. (4,5), then byte 6's first two
+                    uint32_t tmp[17];
+#pragma unroll
+                    for (int jp = 0; jp < 3; ++jp) pair_at(2 * jp, &tmp[5 * jp]);
+                    single_at(6, &tmp[15]);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) hv[i] = tmp[i];
+                } else {  // codes 32..63: byte pairs (6,7) .. (10,11) give codes 30..59, byte 12 codes 60..63
+                    uint32_t tmp[15];
+#pragma unroll
+                    for (int jp = 0; jp < 3; ++jp) pair_at(6 + 2 * jp, &tmp[5 * jp]);
+#pragma unroll
+                    for (int i = 0; i < 14; ++i) hv[i] = tmp[i + 1];
+                    single_at(12, &hv[14]);
+                }
             }
-            if (B & 1) {  // gs=64: byte 12 holds codes 60..63
-                const uint32_t u = lut_of(B - 1) * 16385u;
-                hv[GS / 2 - 2] = wv(u, 0x00030003u, 0);
-                hv[GS / 2 - 1] = wv(u, 0x00300030u, 2);
-            }
-            // store into the stage's A tile (K-major, 128-byte swizzle)
+            // store into the stage's A tile (K-major, 128-byte swizzle): 16-byte
+            // chunk q of this half is chunk (GS/16) h + q of the row
             uint8_t *at = smem + (size_t)s * stage_bytes;
 #pragma unroll
-            for (int chunk = 0; chunk < GS / 8; ++chunk) {
-                uint4 v = make_uint4(hv[4 * chunk], hv[4 * chunk + 1], hv[4 * chunk + 2], hv[4 * chunk + 3]);
+            for (int q = 0; q < GS / 16; ++q) {
+                const int chunk = (GS / 16) * h + q;
+                uint4 v = make_uint4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
                 if (!rok) v = make_uint4(0, 0, 0, 0);
                 *reinterpret_cast<uint4 *>(at + (chunk >> 3) * 16384 + sw128_offset(r, chunk & 7)) = v;
             }
@@ -355,32 +403,37 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
         }
     }
 
-    // ---- epilogue ----------------------------------------------------------------
+    // ---- epilogue: warp w drains TMEM lanes 32 (w % 4) .. +31, column half w / 4 ------
     __syncthreads();
-    if (warp < 4 && steps > 0) wait_bounded(smem_addr(&done_bar), 0);
+    if (warp < kDecodeWarpsQ && steps > 0) wait_bounded(smem_addr(&done_bar), 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const bool ok_all = !abort_flag;
     float *red = reinterpret_cast<float *>(smem);  // split-K partials reuse rank 0's stage ring
     if (S > 1) cluster_sync();                     // every rank's MMAs are complete
-    const int r = (warp & 3) * 32 + lane;
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
     const int row = n0 + r;
-    if (warp < 4 && S > 1 && rank != 0 && steps > 0) {
-        for (int c0 = 0; c0 < p.bx; c0 += 32) {
+    // columns of this warp: half (warp >> 2) of bx, in blocks of 32 (bx = 32: warps 0-3 only)
+    const int cw = p.bx >= 64 ? p.bx / 2 : p.bx;
+    const int c_beg = p.bx >= 64 ? (warp >> 2) * cw : 0;
+    const bool drains = warp < kDecodeWarpsQ && (p.bx >= 64 || warp < 4);
+    if (drains && S > 1 && rank != 0 && steps > 0) {
+        for (int c0 = c_beg; c0 < c_beg + cw; c0 += 32) {
             uint32_t v[32];
-            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+            tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)c0, v);
             float *dst = red + ((size_t)(rank - 1) * 128 + r) * p.bx + c0;
 #pragma unroll
             for (int q = 0; q < 32; ++q) st_cluster_f32(smem_addr(dst + q), 0, __uint_as_float(v[q]));
         }
     }
     if (S > 1) cluster_sync();
-    if (warp < 4 && rank == 0 && ok_all) {
-        for (int c0 = 0; c0 < p.bx; c0 += 32) {
+    if (drains && rank == 0 && ok_all) {
+        for (int c0 = c_beg; c0 < c_beg + cw; c0 += 32) {
             uint32_t v[32];
             if (steps > 0) {
-                tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+                tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)c0, v);
             } else {
 #pragma unroll
                 for (int q = 0; q < 32; ++q) v[q] = 0u;
@@ -397,7 +450,7 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) tmem_dealloc(tmem, (uint32_t)p.bx);
+    if (warp == kMmaWarpQ) tmem_dealloc(tmem, (uint32_t)p.bx);
 }
 
 // ---- host side -------------------------------------------------------------------
@@ -474,7 +527,7 @@ int launch_qmm_t5(const QmvArgs &a, cudaStream_t s)
     p.M = (int)a.M; p.N = (int)a.N; p.K = (int)a.K; p.G = (int)a.G;
     p.row_bytes = a.row_bytes;
     p.zero = 0;
-    p.bx = a.M <= 32 ? 32 : (a.M <= 64 ? 64 : 128);
+    p.bx = a.M <= 32 ? 32 : (a.M <= 64 ? 64 : (a.M <= 128 ? 128 : 256));
     const int n_tiles = (p.N + 127) / 128, m_tiles = (p.M + p.bx - 1) / p.bx;
     const int tiles = n_tiles * m_tiles;
     const int sms = sm_count();
