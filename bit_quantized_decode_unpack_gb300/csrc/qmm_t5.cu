@@ -294,29 +294,44 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
         // the group's bytes (aligned 32-bit loads, realigned with funnel shifts;
         // row_bytes is a multiple of 16 here), scale and bias: the next K step's
         // are requested before this one is decoded
-        constexpr int NW = (B + 3 + 3) / 4;
-        // the group's bytes (aligned 32-bit loads, realigned with funnel shifts;
-        // row_bytes is a multiple of 16 here), scale and bias: the next K step's
-        // are requested before this one is decoded
-        uint32_t raw_n[NW + 1];
-        int sh_n = 0;
+        // The bytes of this thread's half of the group: from byte FB (0, or 12 /
+        // 6 for the second half), NWH words, read as two aligned 16-byte loads
+        // (row_bytes is a multiple of 16 here) and realigned in registers.  The
+        // next K step's bytes, scale and bias are requested before this one is
+        // decoded.
+        constexpr int FB1 = GS == 128 ? 12 : 6;
+        constexpr int NWH = GS == 128 ? 4 : 2;
+        const int fb = h ? FB1 : 0;
+        uint4 w0n = make_uint4(0, 0, 0, 0), w1n = make_uint4(0, 0, 0, 0);
+        int ow_n = 0;
         uint16_t sb_n = 0, bb_n = 0;
         auto fetch = [&](int g) {
-            const long long off = (long long)g * B;
-            const long long aoff = off & ~3LL;
-            const uint32_t *base = reinterpret_cast<const uint32_t *>(wrow + aoff);
-            sh_n = (int)(off & 3) * 8;
-#pragma unroll
-            for (int q = 0; q <= NW; ++q) raw_n[q] = (rok && aoff + 4 * q < p.row_bytes) ? base[q] : 0u;
+            const long long start = (long long)g * B + fb;
+            const long long astart = start & ~15LL;
+            ow_n = (int)(start & 15);
+            w0n = rok ? *reinterpret_cast<const uint4 *>(wrow + astart) : make_uint4(0, 0, 0, 0);
+            w1n = rok && astart + 16 < p.row_bytes ? *reinterpret_cast<const uint4 *>(wrow + astart + 16)
+                                                   : make_uint4(0, 0, 0, 0);
             sb_n = rok ? __half_as_ushort(srow[g]) : (uint16_t)0;
             bb_n = rok && brow ? __half_as_ushort(brow[g]) : (uint16_t)0;
         };
         if (steps > 0) fetch(g_lo);
         for (int it = 0; it < steps; ++it) {
             const int s = it % NST;
-            uint32_t bytes_w[NW];
+            uint32_t bytes_w[NWH];
+            {
+                const uint32_t W[8] = {w0n.x, w0n.y, w0n.z, w0n.w, w1n.x, w1n.y, w1n.z, w1n.w};
+                const int wo = ow_n >> 2, sh = (ow_n & 3) * 8;
+                uint32_t V[NWH + 1];
 #pragma unroll
-            for (int q = 0; q < NW; ++q) bytes_w[q] = __funnelshift_r(raw_n[q], raw_n[q + 1], sh_n);
+                for (int i = 0; i <= NWH; ++i) {
+                    const uint32_t lo = (wo & 1) ? W[i + 1] : W[i];
+                    const uint32_t hi = (wo & 1) ? W[i + 3] : W[i + 2];
+                    V[i] = (wo & 2) ? hi : lo;
+                }
+#pragma unroll
+                for (int q = 0; q < NWH; ++q) bytes_w[q] = __funnelshift_r(V[q], V[q + 1], sh);
+            }
             const uint16_t sb = sb_n;
             const uint16_t bb = rok ? (brow ? bb_n : __half_as_ushort(sym_bias(__ushort_as_half(sb), p.ratio)))
                                     : (uint16_t)0;
@@ -339,7 +354,9 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
                 return hadd2(ts, b2);
             };
             auto lut_of = [&](int j) -> uint32_t { return lut[__byte_perm(bytes_w[j >> 2], 0, 0x4440 | (j & 3))]; };
-            // codes 5j .. 5j+9 of bytes (j, j+1), two per 32-bit word (code 2i low, 2i+1 high)
+            // j below is the byte index within this half's words; codes 5j .. 5j+9
+            // of bytes (j, j+1) (relative to the half's first byte), two per
+            // 32-bit word (code 2i low, 2i+1 high)
             auto pair_at = [&](int j, uint32_t *out) {
                 const uint32_t L0 = lut_of(j), L1 = lut_of(j + 1);
                 const uint32_t u = L0 * 16385u;      // fields of byte j, also shifted by 14
@@ -367,7 +384,7 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
                 } else {  // codes 64..127: byte pairs (12,13) .. (24,25) give codes 60..129
                     uint32_t tmp[35];
 #pragma unroll
-                    for (int jp = 0; jp < 7; ++jp) pair_at(12 + 2 * jp, &tmp[5 * jp]);
+                    for (int jp = 0; jp < 7; ++jp) pair_at(2 * jp, &tmp[5 * jp]);  // local bytes 0..13 = group bytes 12..25
 #pragma unroll
                     for (int i = 0; i < 32; ++i) hv[i] = tmp[i + 2];
                 }
@@ -382,10 +399,10 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
                 } else {  // codes 32..63: byte pairs (6,7) .. (10,11) give codes 30..59, byte 12 codes 60..63
                     uint32_t tmp[15];
 #pragma unroll
-                    for (int jp = 0; jp < 3; ++jp) pair_at(6 + 2 * jp, &tmp[5 * jp]);
+                    for (int jp = 0; jp < 3; ++jp) pair_at(2 * jp, &tmp[5 * jp]);  // local bytes 0..6 = group bytes 6..12
 #pragma unroll
                     for (int i = 0; i < 14; ++i) hv[i] = tmp[i + 1];
-                    single_at(12, &hv[14]);
+                    single_at(6, &hv[14]);
                 }
             }
             // store into the stage's A tile (K-major, 128-byte swizzle): 16-byte
@@ -518,7 +535,8 @@ int take_qmm_timeouts(unsigned int *count)
 int launch_qmm_t5(const QmvArgs &a, cudaStream_t s)
 {
     if (a.fmt != BQD_FMT_T5) return BQD_ERR_UNSUPPORTED;
-    if (a.row_bytes % 16 != 0) return BQD_ERR_UNSUPPORTED;  // aligned 32-bit byte loads stay inside a row
+    // the decode reads 16-byte aligned pieces of each row
+    if (a.row_bytes % 16 != 0 || (reinterpret_cast<uintptr_t>(a.w) & 15)) return BQD_ERR_UNSUPPORTED;
     if (a.K > (int64_t)1 << 30 || a.N > (int64_t)1 << 30 || a.M > (int64_t)1 << 30) return BQD_ERR_UNSUPPORTED;
     auto enc = encode_fn();
     if (!enc) return BQD_ERR_UNSUPPORTED;
