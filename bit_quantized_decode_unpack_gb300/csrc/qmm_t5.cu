@@ -51,7 +51,8 @@ constexpr int kMmaWarpQ = kDecodeWarpsQ;                // TMEM owner, MMA issue
 constexpr int kTmaWarpQ = kDecodeWarpsQ + 1;            // x tiles by TMA
 constexpr int kThreadsQ = (kDecodeWarpsQ + 2) * 32;
 constexpr int kMaxStagesQ = 8;
-constexpr size_t kQmmSmemMax = 220 * 1024;
+constexpr size_t kQmmSmemMax = 208 * 1024;  // dynamic; the replicated decode table is static
+constexpr int kLutCopiesQ = 16;              // lane l reads copy l % 16: fewer bank conflicts
 
 __device__ unsigned int g_qmm_timeouts = 0;
 
@@ -183,7 +184,7 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t x_full[kMaxStagesQ], a_full[kMaxStagesQ], empty_bar[kMaxStagesQ], done_bar;
     __shared__ uint32_t tmem_base;
-    __shared__ uint32_t lut[256];
+    __shared__ uint32_t lut[256 * kLutCopiesQ];  // entry v of copy c at v * 16 + c
     __shared__ int abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -203,8 +204,8 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t stage_bytes = A_BYTES + X_BYTES;
 
-    for (int q = tid; q < 256; q += kThreadsQ) {
-        int v = q, e = 0;
+    for (int q = tid; q < 256 * kLutCopiesQ; q += kThreadsQ) {
+        int v = q / kLutCopiesQ, e = 0;
         if (v < 243)
             for (int d = 0; d < 5; ++d) {
                 e |= (v % 3) << (2 * d);
@@ -353,7 +354,9 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
                 const uint32_t ts = fast ? hfma2(hh, s2, c[d]) : hmul2(hsub2(hh, mg[d]), s2);  // t*s, exact
                 return hadd2(ts, b2);
             };
-            auto lut_of = [&](int j) -> uint32_t { return lut[__byte_perm(bytes_w[j >> 2], 0, 0x4440 | (j & 3))]; };
+            auto lut_of = [&](int j) -> uint32_t {
+                return lut[__byte_perm(bytes_w[j >> 2], 0, 0x4440 | (j & 3)) * kLutCopiesQ + (lane & (kLutCopiesQ - 1))];
+            };
             // j below is the byte index within this half's words; codes 5j .. 5j+9
             // of bytes (j, j+1) (relative to the half's first byte), two per
             // 32-bit word (code 2i low, 2i+1 high)
