@@ -12,8 +12,9 @@ weights + fp16 scales + fp16 biases (0 for sym and t5) + fp16 x + fp16 y.
 `value` is device-resident throughput (bytes of all calls / device time);
 `e2e` is the same through the same C-ABI calls with activations copied from
 pinned host memory and results copied back inside the timed region; the
-weights are the model's resident state.  The t5 prefill matrix product is
-timed separately (key "qmm"), in TFLOP/s.
+weights are the model's resident state.  The prefill matrix product is
+timed separately in TFLOP/s: t5 (key "qmm"), 2-bit and 1-bit affine with
+biases (keys "qmm_affine2", "qmm_affine1").
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -313,34 +314,41 @@ def per_call_table(sweep, reps: int = 3):
 QMM_CASES = [(M, N, K) for M in (32, 512, 2048) for (N, K) in [(17408, 5120), (5120, 17408)]]
 
 
-def time_qmm(dev, reps: int = 10):
-    """t5 prefill matrix product (M > 16 -> tcgen05 kernel), gs=128: TFLOP/s
-    per case (2*M*N*K flops), each case over two rotating weight sets."""
+def time_qmm(dev, fmt: int, reps: int = 10):
+    """Prefill matrix product (M > 16 -> tcgen05 kernel) of one format, gs=128:
+    TFLOP/s per case (2*M*N*K flops).  Each case rotates through enough weight
+    sets (codes, scales, biases for 1/2-bit) to exceed the 129 MB L2."""
     import torch
     import bit_quantized_decode_unpack_gb300 as bqd
     from bit_quantized_decode_unpack_gb300 import synth
     gen = torch.Generator(device=dev)
-    gen.manual_seed(77)
+    gen.manual_seed(77 + fmt)
     rows, tot_flop, tot_ms = [], 0.0, 0.0
     for M, N, K in QMM_CASES:
+        set_bytes = bqd.packed_bytes(fmt, N, K, 128) + N * (K // 128) * 2 * (1 if fmt == T5 else 2)
+        nsets = max(2, -(-160 * 2**20 // set_bytes))
         W = []
-        for _ in range(2):
+        for _ in range(nsets):
             s_ = synth.torch_scales(gen, N, K // 128, dev)
-            W.append((bqd.pack(synth.torch_codes(gen, T5, N, K, dev), T5, 128), s_))
+            b_ = synth.torch_biases(gen, fmt, s_, dev)
+            W.append((bqd.pack(synth.torch_codes(gen, fmt, N, K, dev), fmt, 128), s_, b_))
         x = synth.torch_activations(gen, M, K, dev)
         y = torch.empty(M, N, dtype=torch.float16, device=dev)
         for i in range(3):
-            bqd.qmv(x, W[i % 2][0], W[i % 2][1], None, T5, 128, out=y)
+            w_, s_, b_ = W[i % nsets]
+            bqd.qmv(x, w_, s_, b_, fmt, 128, out=y)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for i in range(reps):
-            bqd.qmv(x, W[i % 2][0], W[i % 2][1], None, T5, 128, out=y)
+            w_, s_, b_ = W[i % nsets]
+            bqd.qmv(x, w_, s_, b_, fmt, 128, out=y)
         e1.record()
         e1.synchronize()
         ms = e0.elapsed_time(e1) / reps
         flop = 2.0 * M * N * K
-        rows.append({"M": M, "N": N, "K": K, "us": round(ms * 1e3, 1), "tflops": round(flop / (ms * 1e-3) / 1e12, 1)})
+        rows.append({"M": M, "N": N, "K": K, "us": round(ms * 1e3, 1), "tflops": round(flop / (ms * 1e-3) / 1e12, 1),
+                     "weight_sets": nsets})
         tot_flop += flop
         tot_ms += ms
         del W, x, y
@@ -487,7 +495,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="two projections only (development)")
     ap.add_argument("--table", type=str, default=None, help="write the per-call table (CSV) here")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-qmm", action="store_true", help="skip the t5 prefill matrix-product timing")
+    ap.add_argument("--no-qmm", action="store_true", help="skip the prefill matrix-product timings")
     ap.add_argument("--cpu-rows", type=int, default=0, help="0: sized for ~12 s of oracle work")
     ap.add_argument("--case", type=str, default=None, help="fmt,M,N,K,gs[,sym]: time one configuration")
     args = ap.parse_args()
@@ -565,12 +573,15 @@ def main():
             "clocks": clocks,
         }
         if not args.no_qmm:
-            qrows, qagg = time_qmm(dev)
             tf_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-            line["qmm"] = {"metric": "t5 prefill QMM TFLOP/s (2*M*N*K), gs=128", "value": qagg, "unit": "TFLOP/s",
-                           "cases": qrows,
-                           "roofline": {"bound": "tensor", "achieved": qagg, "peak": tf_peak, "unit": "TFLOP/s",
-                                        "frac": qagg / tf_peak, "peak_source": src + " bf16 burst (fp16 runs at the bf16 rate)"}}
+            for key, fmt, label in (("qmm", T5, "t5"), ("qmm_affine2", F2, "2-bit affine"),
+                                    ("qmm_affine1", F1, "1-bit affine")):
+                qrows, qagg = time_qmm(dev, fmt)
+                line[key] = {"metric": f"{label} prefill QMM TFLOP/s (2*M*N*K), gs=128", "value": qagg,
+                             "unit": "TFLOP/s", "cases": qrows,
+                             "roofline": {"bound": "tensor", "achieved": qagg, "peak": tf_peak, "unit": "TFLOP/s",
+                                          "frac": qagg / tf_peak,
+                                          "peak_source": src + " bf16 burst (fp16 runs at the bf16 rate)"}}
         if not args.no_cpu_baseline:
             import oracle
             oracle.build()

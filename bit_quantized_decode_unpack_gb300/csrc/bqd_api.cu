@@ -23,17 +23,18 @@ int sm_count()
     return cached[dev];
 }
 
-// Testing override of the dispatcher: BQD_FORCE_KERNEL=generic|mma|tma (read
-// on every call so that a test can compare the kernels in one process).
-// "mma" forces the register-streaming tensor-core kernels, "tma" the
-// TMA-ring kernels (1/2-bit and t5 decode); a forced kernel's "unsupported"
-// is returned as is.
+// Testing override of the dispatcher: BQD_FORCE_KERNEL=generic|mma|tma|qmm
+// (read on every call so that a test can compare the kernels in one process).
+// "mma" forces the register-streaming tensor-core kernels (the prefill
+// product for M > 16), "tma" the TMA-ring decode kernels, "qmm" the tcgen05
+// prefill product at any M; a forced kernel's "unsupported" is returned as is.
 static int forced_kernel()
 {
     const char *v = getenv("BQD_FORCE_KERNEL");
     if (v && strcmp(v, "generic") == 0) return 1;
     if (v && strcmp(v, "mma") == 0) return 2;
     if (v && strcmp(v, "tma") == 0) return 3;
+    if (v && strcmp(v, "qmm") == 0) return 4;
     return 0;
 }
 
@@ -103,10 +104,10 @@ static int qmv_common(const void *x, const void *w, const void *scales, const vo
 
     const int force = forced_kernel();
     if (force != 1) {
-        // t5 prefill (M > 16): fused unpack + tcgen05 matrix product
-        if (format == BQD_FMT_T5 && M > 16) {
-            int st = launch_qmm_t5(a, s);
-            if (st != BQD_ERR_UNSUPPORTED || force == 2) return st;
+        // prefill (M > 16): fused unpack + tcgen05 matrix product
+        if (M > 16 || force == 4) {
+            int st = launch_qmm(a, s);
+            if (st != BQD_ERR_UNSUPPORTED || force == 2 || force == 4) return st;
         }
         if (force != 2) {
             // TMA-ring kernels (1/2-bit: K a multiple of 256; t5: of 1024;

@@ -1,11 +1,14 @@
-// t5 prefill matrix product on the 5th-generation tensor cores (tcgen05).
+// Prefill matrix product of packed weights on the 5th-generation tensor cores
+// (tcgen05), for the t5 ternary format and the 1/2-bit affine formats.
 //
 // Page: "oMLX Bonsai 自定义内核:Qwen 系列快速 QMV 路径完整解析", §二.3: for long
 // prefill (M > 16) t5 weights go through a fused "unpack + matrix multiply"
-// kernel (bonsai_t5_qmm) that reads every t5 byte once.
+// kernel (bonsai_t5_qmm) that reads every t5 byte once.  §二.1 notes that the
+// 1-bit prefill path had no such kernel (it dequantised to float16 and called
+// a dense matmul); here the 1/2-bit formats take the same fused product.
 //
-//   Y[m, n] = sum_k X[m, k] * W[n, k],  W[n, k] = fp16(s[n,g] * t[n,k] + b[n,g])
-//   (sym: b = fp16(-ratio * s), default ratio 1 -> W = s*(t-1), exact in fp16)
+//   Y[m, n] = sum_k X[m, k] * W[n, k],  W[n, k] = fp16(fp16(s[n,g] * q[n,k]) + b[n,g])
+//   (sym: b = fp16(-ratio * s); t5 with the default ratio 1 gives W = s*(t-1))
 //
 // One CTA owns 128 weight rows x BX activation rows (BX = 32, 64, 128 or 256)
 // and a range of K groups.  When the (weight, activation) tiles are too few to
@@ -15,14 +18,21 @@
 //
 // Roles (320 threads):
 //   warps 0-7  decode: thread (r, h) = (tid % 128, warp / 4) decodes half h of
-//              weight row n0+r's group per K step (one group of gs codes):
-//              codes [0, gs/2) or [gs/2, gs), both starting on an even byte,
-//              so byte pairs decode as a unit.  It loads the group's t5 bytes,
-//              decodes them with a shared byte->trits table, forms the fp16
-//              weights (magic-exponent LOP3 + HFMA2 gives s*t exactly, then
-//              + b) and stores them into the stage's A tile in the tcgen05
-//              K-major 128-byte-swizzled layout.  After the K loop warp w
-//              drains TMEM lanes 32(w%4)..+31, columns of half w/4, and stores Y.
+//              weight row n0+r's group per K step (one group of gs codes),
+//              forms the fp16 weights and stores them into the stage's A tile
+//              in the tcgen05 K-major 128-byte-swizzled layout.
+//              t5: codes [0, gs/2) or [gs/2, gs), both starting on an even
+//              byte, so byte pairs decode as a unit: the group's t5 bytes go
+//              through a shared byte->trits table, then a magic-exponent LOP3
+//              + HFMA2 give s*t exactly, then + b.
+//              1/2-bit: the half group is one aligned 4-, 8- or 16-byte load;
+//              a byte is duplicated into both 16-bit halves of a word, and one
+//              LOP3 per code pair places code 2i in the low half and code 2i+1
+//              in the high half at different mantissa positions (offsets
+//              2^(10-p) per half), so HFMA2 against per-half constants gives
+//              (s*q_2i, s*q_2i+1) in natural K order, then + b.
+//              After the K loop warp w drains TMEM lanes 32(w%4)..+31,
+//              columns of half w/4, and stores Y.
 //   warp 8     allocates TMEM; lane 0 issues tcgen05.mma (kind::f16, M=128,
 //              N=BX, K=16, fp32 accumulation in TMEM) and tcgen05.commit, which
 //              frees a stage once its MMAs have completed.
@@ -174,17 +184,18 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c)
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-template <int GS>
-__global__ void __launch_bounds__(kThreadsQ, 1)
-qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
+template <int FMT, int GS>
+__device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParams &p)
 {
+    constexpr bool T5F = FMT == BQD_FMT_T5;
     constexpr int B = GS == 64 ? 13 : 26;  // t5 bytes per group
     constexpr int NSUB = GS / 64;          // 64-code sub-tiles per K step
     constexpr int A_BYTES = 128 * GS * 2;  // A tile per stage
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t x_full[kMaxStagesQ], a_full[kMaxStagesQ], empty_bar[kMaxStagesQ], done_bar;
     __shared__ uint32_t tmem_base;
-    __shared__ uint32_t lut[256 * kLutCopiesQ];  // entry v of copy c at v * 16 + c
+    // t5 byte -> trits table, entry v of copy c at v * 16 + c (1/2-bit: unused)
+    __shared__ uint32_t lut[T5F ? 256 * kLutCopiesQ : 1];
     __shared__ int abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -204,14 +215,16 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t stage_bytes = A_BYTES + X_BYTES;
 
-    for (int q = tid; q < 256 * kLutCopiesQ; q += kThreadsQ) {
-        int v = q / kLutCopiesQ, e = 0;
-        if (v < 243)
-            for (int d = 0; d < 5; ++d) {
-                e |= (v % 3) << (2 * d);
-                v /= 3;
-            }
-        lut[q] = (uint32_t)e;
+    if constexpr (T5F) {
+        for (int q = tid; q < 256 * kLutCopiesQ; q += kThreadsQ) {
+            int v = q / kLutCopiesQ, e = 0;
+            if (v < 243)
+                for (int d = 0; d < 5; ++d) {
+                    e |= (v % 3) << (2 * d);
+                    v /= 3;
+                }
+            lut[q] = (uint32_t)e;
+        }
     }
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
@@ -289,38 +302,63 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
         const uint8_t *wrow = p.w + (long long)(rok ? row : 0) * p.row_bytes;
         const __half *srow = p.scales + (long long)(rok ? row : 0) * p.G;
         const __half *brow = p.biases ? p.biases + (long long)(rok ? row : 0) * p.G : nullptr;
-        uint32_t mg[5];
-#pragma unroll
-        for (int d = 0; d < 5; ++d) mg[d] = magic(2 * d) ^ p.zero;
-        // the group's bytes (aligned 32-bit loads, realigned with funnel shifts;
-        // row_bytes is a multiple of 16 here), scale and bias: the next K step's
-        // are requested before this one is decoded
-        // The bytes of this thread's half of the group: from byte FB (0, or 12 /
-        // 6 for the second half), NWH words, read as two aligned 16-byte loads
-        // (row_bytes is a multiple of 16 here) and realigned in registers.  The
-        // next K step's bytes, scale and bias are requested before this one is
-        // decoded.
+        // t5: the bytes of this thread's half of the group, from byte FB (0, or
+        // 12 / 6 for the second half), NWH words, read as two aligned 16-byte
+        // loads (row_bytes is a multiple of 16 here) and realigned in registers.
         constexpr int FB1 = GS == 128 ? 12 : 6;
         constexpr int NWH = GS == 128 ? 4 : 2;
+        // 1/2-bit: the half group is HB bytes (HW words) at byte g*2HB + h*HB,
+        // one aligned load (row_bytes = G * 2HB and the base is 16-byte aligned)
+        constexpr int CPB = FMT == BQD_FMT_AFFINE2 ? 4 : 8;  // codes per byte
+        constexpr int HB = GS / (2 * CPB);                   // 4, 8 or 16
+        constexpr int HW = T5F ? NWH : HB / 4;               // words decoded per step
         const int fb = h ? FB1 : 0;
         uint4 w0n = make_uint4(0, 0, 0, 0), w1n = make_uint4(0, 0, 0, 0);
         int ow_n = 0;
+        uint32_t an[T5F ? 1 : HW];
         uint16_t sb_n = 0, bb_n = 0;
+        // the next K step's bytes, scale and bias are requested before the
+        // current one is decoded
         auto fetch = [&](int g) {
-            const long long start = (long long)g * B + fb;
-            const long long astart = start & ~15LL;
-            ow_n = (int)(start & 15);
-            w0n = rok ? *reinterpret_cast<const uint4 *>(wrow + astart) : make_uint4(0, 0, 0, 0);
-            w1n = rok && astart + 16 < p.row_bytes ? *reinterpret_cast<const uint4 *>(wrow + astart + 16)
-                                                   : make_uint4(0, 0, 0, 0);
+            if constexpr (T5F) {
+                const long long start = (long long)g * B + fb;
+                const long long astart = start & ~15LL;
+                ow_n = (int)(start & 15);
+                w0n = rok ? *reinterpret_cast<const uint4 *>(wrow + astart) : make_uint4(0, 0, 0, 0);
+                w1n = rok && astart + 16 < p.row_bytes ? *reinterpret_cast<const uint4 *>(wrow + astart + 16)
+                                                       : make_uint4(0, 0, 0, 0);
+            } else {
+                const uint8_t *src = wrow + (long long)g * (2 * HB) + h * HB;
+                if constexpr (HW == 4) {
+                    const uint4 v = rok ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0, 0, 0, 0);
+                    an[0] = v.x; an[1] = v.y; an[2] = v.z; an[3] = v.w;
+                } else if constexpr (HW == 2) {
+                    const uint2 v = rok ? *reinterpret_cast<const uint2 *>(src) : make_uint2(0, 0);
+                    an[0] = v.x; an[1] = v.y;
+                } else {
+                    an[0] = rok ? *reinterpret_cast<const uint32_t *>(src) : 0u;
+                }
+            }
             sb_n = rok ? __half_as_ushort(srow[g]) : (uint16_t)0;
             bb_n = rok && brow ? __half_as_ushort(brow[g]) : (uint16_t)0;
         };
+        // magic exponents: t5 fields sit at bits 2d of both halves; 1/2-bit
+        // pair d has its low code at mantissa bit PLO(d), its high one at PHI(d)
+        uint32_t mg[5];
+#pragma unroll
+        for (int d = 0; d < 5; ++d) mg[d] = magic(2 * d) ^ p.zero;
+        constexpr int NPAT = FMT == BQD_FMT_AFFINE2 ? 2 : 4;  // 1/2-bit pair patterns per byte
+        auto plo = [](int d) { return FMT == BQD_FMT_AFFINE2 ? 4 * d : 2 * d; };
+        auto phi = [](int d) { return FMT == BQD_FMT_AFFINE2 ? 4 * d + 2 : 2 * d + 1; };
+        uint32_t mgx[NPAT];
+#pragma unroll
+        for (int d = 0; d < NPAT; ++d)
+            mgx[d] = ((magic(plo(d)) & 0xFFFFu) | (magic(phi(d)) & 0xFFFF0000u)) ^ p.zero;
         if (steps > 0) fetch(g_lo);
         for (int it = 0; it < steps; ++it) {
             const int s = it % NST;
-            uint32_t bytes_w[NWH];
-            {
+            uint32_t cur[HW];
+            if constexpr (T5F) {
                 const uint32_t W[8] = {w0n.x, w0n.y, w0n.z, w0n.w, w1n.x, w1n.y, w1n.z, w1n.w};
                 const int wo = ow_n >> 2, sh = (ow_n & 3) * 8;
                 uint32_t V[NWH + 1];
@@ -331,7 +369,10 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
                     V[i] = (wo & 2) ? hi : lo;
                 }
 #pragma unroll
-                for (int q = 0; q < NWH; ++q) bytes_w[q] = __funnelshift_r(V[q], V[q + 1], sh);
+                for (int q = 0; q < NWH; ++q) cur[q] = __funnelshift_r(V[q], V[q + 1], sh);
+            } else {
+#pragma unroll
+                for (int q = 0; q < HW; ++q) cur[q] = an[q];
             }
             const uint16_t sb = sb_n;
             const uint16_t bb = rok ? (brow ? bb_n : __half_as_ushort(sym_bias(__ushort_as_half(sb), p.ratio)))
@@ -342,71 +383,100 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
                 break;
             }
             const uint32_t s2 = dup_half(sb), b2 = dup_half(bb);
-            // constants -2^(10-2d)*s stay finite for |s| < 63; else the exact
+            // constants -2^(10-p)*s stay finite for |s| < 63; else the exact
             // (magic - offset) * s form is used
             const bool fast = fabsf(__half2float(__ushort_as_half(sb))) < 63.f;
-            uint32_t c[5];
-#pragma unroll
-            for (int d = 0; d < 5; ++d)
-                c[d] = hmul2(s2, dup_half(__half_as_ushort(__float2half_rn(-(float)(1024 >> (2 * d))))));
-            auto wv = [&](uint32_t field_word, uint32_t mask, int d) -> uint32_t {
-                const uint32_t hh = (field_word & mask) | mg[d];
-                const uint32_t ts = fast ? hfma2(hh, s2, c[d]) : hmul2(hsub2(hh, mg[d]), s2);  // t*s, exact
-                return hadd2(ts, b2);
-            };
-            auto lut_of = [&](int j) -> uint32_t {
-                return lut[__byte_perm(bytes_w[j >> 2], 0, 0x4440 | (j & 3)) * kLutCopiesQ + (lane & (kLutCopiesQ - 1))];
-            };
-            // j below is the byte index within this half's words; codes 5j .. 5j+9
-            // of bytes (j, j+1) (relative to the half's first byte), two per
-            // 32-bit word (code 2i low, 2i+1 high)
-            auto pair_at = [&](int j, uint32_t *out) {
-                const uint32_t L0 = lut_of(j), L1 = lut_of(j + 1);
-                const uint32_t u = L0 * 16385u;      // fields of byte j, also shifted by 14
-                const uint32_t u2 = L0 + (L1 << 24);  // (trit 4 of byte j, trit 0 of byte j+1) at bit 8
-                const uint32_t u3 = L1 * 16385u;     // fields of byte j+1, also shifted by 14
-                out[0] = wv(u, 0x00030003u, 0);
-                out[1] = wv(u, 0x00300030u, 2);
-                out[2] = wv(u2, 0x03000300u, 4);
-                out[3] = wv(u3, 0x000C000Cu, 1);
-                out[4] = wv(u3, 0x00C000C0u, 3);
-            };
-            // codes 5j .. 5j+3 of a lone byte j
-            auto single_at = [&](int j, uint32_t *out) {
-                const uint32_t u = lut_of(j) * 16385u;
-                out[0] = wv(u, 0x00030003u, 0);
-                out[1] = wv(u, 0x00300030u, 2);
-            };
-            // this thread's GS/4 words (GS/2 codes): half h of the group
+            // this thread's GS/4 words (GS/2 codes, two per word: code 2i low,
+            // 2i+1 high): half h of the group
             uint32_t hv[GS / 4];
-            if (GS == 128) {
-                if (h == 0) {  // codes 0..63: byte pairs (0,1) .. (10,11), then byte 12's first four
+            if constexpr (T5F) {
+                uint32_t c[5];
 #pragma unroll
-                    for (int jp = 0; jp < 6; ++jp) pair_at(2 * jp, &hv[5 * jp]);
-                    single_at(12, &hv[30]);
-                } else {  // codes 64..127: byte pairs (12,13) .. (24,25) give codes 60..129
-                    uint32_t tmp[35];
+                for (int d = 0; d < 5; ++d)
+                    c[d] = hmul2(s2, dup_half(__half_as_ushort(__float2half_rn(-(float)(1024 >> (2 * d))))));
+                auto wv = [&](uint32_t field_word, uint32_t mask, int d) -> uint32_t {
+                    const uint32_t hh = (field_word & mask) | mg[d];
+                    const uint32_t ts = fast ? hfma2(hh, s2, c[d]) : hmul2(hsub2(hh, mg[d]), s2);  // t*s, exact
+                    return hadd2(ts, b2);
+                };
+                auto lut_of = [&](int j) -> uint32_t {
+                    return lut[__byte_perm(cur[j >> 2], 0, 0x4440 | (j & 3)) * kLutCopiesQ +
+                               (lane & (kLutCopiesQ - 1))];
+                };
+                // j below is the byte index within this half's words; codes 5j .. 5j+9
+                // of bytes (j, j+1) (relative to the half's first byte)
+                auto pair_at = [&](int j, uint32_t *out) {
+                    const uint32_t L0 = lut_of(j), L1 = lut_of(j + 1);
+                    const uint32_t u = L0 * 16385u;      // fields of byte j, also shifted by 14
+                    const uint32_t u2 = L0 + (L1 << 24);  // (trit 4 of byte j, trit 0 of byte j+1) at bit 8
+                    const uint32_t u3 = L1 * 16385u;     // fields of byte j+1, also shifted by 14
+                    out[0] = wv(u, 0x00030003u, 0);
+                    out[1] = wv(u, 0x00300030u, 2);
+                    out[2] = wv(u2, 0x03000300u, 4);
+                    out[3] = wv(u3, 0x000C000Cu, 1);
+                    out[4] = wv(u3, 0x00C000C0u, 3);
+                };
+                // codes 5j .. 5j+3 of a lone byte j
+                auto single_at = [&](int j, uint32_t *out) {
+                    const uint32_t u = lut_of(j) * 16385u;
+                    out[0] = wv(u, 0x00030003u, 0);
+                    out[1] = wv(u, 0x00300030u, 2);
+                };
+                if (GS == 128) {
+                    if (h == 0) {  // codes 0..63: byte pairs (0,1) .. (10,11), then byte 12's first four
 #pragma unroll
-                    for (int jp = 0; jp < 7; ++jp) pair_at(2 * jp, &tmp[5 * jp]);  // local bytes 0..13 = group bytes 12..25
+                        for (int jp = 0; jp < 6; ++jp) pair_at(2 * jp, &hv[5 * jp]);
+                        single_at(12, &hv[30]);
+                    } else {  // codes 64..127: byte pairs (12,13) .. (24,25) give codes 60..129
+                        uint32_t tmp[35];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) hv[i] = tmp[i + 2];
+                        for (int jp = 0; jp < 7; ++jp) pair_at(2 * jp, &tmp[5 * jp]);  // local bytes 0..13 = group bytes 12..25
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) hv[i] = tmp[i + 2];
+                    }
+                } else {
+                    if (h == 0) {  // codes 0..31: byte pairs (0,1) .. (4,5), then byte 6's first two
+                        uint32_t tmp[17];
+#pragma unroll
+                        for (int jp = 0; jp < 3; ++jp) pair_at(2 * jp, &tmp[5 * jp]);
+                        single_at(6, &tmp[15]);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) hv[i] = tmp[i];
+                    } else {  // codes 32..63: byte pairs (6,7) .. (10,11) give codes 30..59, byte 12 codes 60..63
+                        uint32_t tmp[15];
+#pragma unroll
+                        for (int jp = 0; jp < 3; ++jp) pair_at(2 * jp, &tmp[5 * jp]);  // local bytes 0..6 = group bytes 6..12
+#pragma unroll
+                        for (int i = 0; i < 14; ++i) hv[i] = tmp[i + 1];
+                        single_at(6, &hv[14]);
+                    }
                 }
             } else {
-                if (h == 0) {  // codes 0..31: byte pairs (0,1) .. (4,5), then byte 6's first two
-                    uint32_t tmp[17];
+                uint32_t c[NPAT];
 #pragma unroll
-                    for (int jp = 0; jp < 3; ++jp) pair_at(2 * jp, &tmp[5 * jp]);
-                    single_at(6, &tmp[15]);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) hv[i] = tmp[i];
-                } else {  // codes 32..63: byte pairs (6,7) .. (10,11) give codes 30..59, byte 12 codes 60..63
-                    uint32_t tmp[15];
-#pragma unroll
-                    for (int jp = 0; jp < 3; ++jp) pair_at(2 * jp, &tmp[5 * jp]);  // local bytes 0..6 = group bytes 6..12
-#pragma unroll
-                    for (int i = 0; i < 14; ++i) hv[i] = tmp[i + 1];
-                    single_at(6, &hv[14]);
+                for (int d = 0; d < NPAT; ++d) {
+                    const uint32_t off = (uint32_t)__half_as_ushort(__float2half_rn(-(float)(1024 >> plo(d)))) |
+                                         ((uint32_t)__half_as_ushort(__float2half_rn(-(float)(1024 >> phi(d)))) << 16);
+                    c[d] = hmul2(s2, off);
                 }
+                // byte y of word q holds codes CPB*(4q+y) ..; it is copied into both
+                // 16-bit halves, and pattern d takes the low half's code at bit
+                // PLO(d) and the high half's at PHI(d) (pair 2-bit: codes 4y+2d,
+                // 4y+2d+1; 1-bit: codes 8y+2d, 8y+2d+1)
+#pragma unroll
+                for (int q = 0; q < HW; ++q)
+#pragma unroll
+                    for (int y = 0; y < 4; ++y) {
+                        const uint32_t dup = __byte_perm(cur[q], 0, 0x4040u | (uint32_t)y | ((uint32_t)y << 8));
+#pragma unroll
+                        for (int d = 0; d < NPAT; ++d) {
+                            const uint32_t mask = (1u << plo(d)) * (CPB == 4 ? 3u : 1u) |
+                                                  ((1u << phi(d)) * (CPB == 4 ? 3u : 1u)) << 16;
+                            const uint32_t hh = (dup & mask) | mgx[d];
+                            const uint32_t qs = fast ? hfma2(hh, s2, c[d]) : hmul2(hsub2(hh, mgx[d]), s2);
+                            hv[(CPB / 2) * (4 * q + y) + d] = hadd2(qs, b2);
+                        }
+                    }
             }
             // store into the stage's A tile (K-major, 128-byte swizzle): 16-byte
             // chunk q of this half is chunk (GS/16) h + q of the row
@@ -473,6 +543,20 @@ qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
     if (warp == kMmaWarpQ) tmem_dealloc(tmem, (uint32_t)p.bx);
 }
 
+template <int GS>
+__global__ void __launch_bounds__(kThreadsQ, 1)
+qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
+{
+    qmm_body<BQD_FMT_T5, GS>(xmap, p);
+}
+
+template <int FMT, int GS>
+__global__ void __launch_bounds__(kThreadsQ, 1)
+qmm_affine_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
+{
+    qmm_body<FMT, GS>(xmap, p);
+}
+
 // ---- host side -------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -490,10 +574,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-template <int GS>
+template <int FMT, int GS>
 int launch_gs(const QmmParams &p, const CUtensorMap &map, int tiles, size_t smem, cudaStream_t s)
 {
-    auto kern = qmm_t5_kernel<GS>;
+    void (*kern)(const CUtensorMap, const QmmParams);
+    if constexpr (FMT == BQD_FMT_T5)
+        kern = qmm_t5_kernel<GS>;
+    else
+        kern = qmm_affine_kernel<FMT, GS>;
     static int configured_dev[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -535,11 +623,13 @@ int take_qmm_timeouts(unsigned int *count)
     return BQD_OK;
 }
 
-int launch_qmm_t5(const QmvArgs &a, cudaStream_t s)
+int launch_qmm(const QmvArgs &a, cudaStream_t s)
 {
-    if (a.fmt != BQD_FMT_T5) return BQD_ERR_UNSUPPORTED;
-    // the decode reads 16-byte aligned pieces of each row
-    if (a.row_bytes % 16 != 0 || (reinterpret_cast<uintptr_t>(a.w) & 15)) return BQD_ERR_UNSUPPORTED;
+    // the decode reads 16-byte aligned pieces of each t5 row; a 1/2-bit half
+    // group is 4, 8 or 16 bytes at a multiple of its size (row_bytes = G * gs/4
+    // or G * gs/8), aligned once the base is
+    if (a.fmt == BQD_FMT_T5 && a.row_bytes % 16 != 0) return BQD_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(a.w) & 15) return BQD_ERR_UNSUPPORTED;
     if (a.K > (int64_t)1 << 30 || a.N > (int64_t)1 << 30 || a.M > (int64_t)1 << 30) return BQD_ERR_UNSUPPORTED;
     auto enc = encode_fn();
     if (!enc) return BQD_ERR_UNSUPPORTED;
@@ -576,9 +666,16 @@ int launch_qmm_t5(const QmvArgs &a, cudaStream_t s)
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return BQD_ERR_CUDA;
     if (getenv("BQD_DEBUG_PLAN"))
-        fprintf(stderr, "bqd qmm plan: M=%d N=%d K=%d gs=%d -> bx=%d tiles=%d S=%d gpr=%d stages=%d smem=%zu\n", p.M,
-                p.N, p.K, a.gs, p.bx, tiles, S, p.gpr, p.stages, smem);
-    return a.gs == 64 ? launch_gs<64>(p, map, tiles, smem, s) : launch_gs<128>(p, map, tiles, smem, s);
+        fprintf(stderr, "bqd qmm plan: fmt=%d M=%d N=%d K=%d gs=%d -> bx=%d tiles=%d S=%d gpr=%d stages=%d smem=%zu\n",
+                a.fmt, p.M, p.N, p.K, a.gs, p.bx, tiles, S, p.gpr, p.stages, smem);
+    if (a.fmt == BQD_FMT_T5)
+        return a.gs == 64 ? launch_gs<BQD_FMT_T5, 64>(p, map, tiles, smem, s)
+                          : launch_gs<BQD_FMT_T5, 128>(p, map, tiles, smem, s);
+    if (a.fmt == BQD_FMT_AFFINE2)
+        return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE2, 64>(p, map, tiles, smem, s)
+                          : launch_gs<BQD_FMT_AFFINE2, 128>(p, map, tiles, smem, s);
+    return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE1, 64>(p, map, tiles, smem, s)
+                      : launch_gs<BQD_FMT_AFFINE1, 128>(p, map, tiles, smem, s);
 }
 
 }  // namespace bqd

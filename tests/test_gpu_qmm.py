@@ -1,8 +1,10 @@
-"""GPU parity of the t5 prefill matrix product (tcgen05 tensor cores, M > 16)
-against the float64 oracle, through the C ABI.
+"""GPU parity of the prefill matrix product (tcgen05 tensor cores, M > 16)
+against the float64 oracle, through the C ABI: t5 and the 1/2-bit formats.
 
 Page: "oMLX Bonsai 自定义内核:Qwen 系列快速 QMV 路径完整解析" §二.3 -- for M > 16
-the t5 weights go through a fused unpack + matrix-multiply kernel.
+the t5 weights go through a fused unpack + matrix-multiply kernel; §二.1 -- the
+1-bit prefill path is a separate (there: dequantise + dense) product, here the
+same fused kernel with a 1/2-bit decode.
 Bar: |y_gpu - y| <= 2e-3 * sum_k |x_k w_k| for every checked output.
 """
 import numpy as np
@@ -14,20 +16,20 @@ from bit_quantized_decode_unpack_gb300 import synth
 from _util import assert_within_tolerance, forced_kernel, to_dev
 
 pytestmark = pytest.mark.gpu
-T5, F2 = bqd.FMT_T5, bqd.FMT_AFFINE2
+T5, F1, F2 = bqd.FMT_T5, bqd.FMT_AFFINE1, bqd.FMT_AFFINE2
 
 
 def run(p, kernel="mma", m_rows=None, n_rows=None):
     import torch
-    gs = p["gs"]
-    w = bqd.pack(to_dev(p["codes"]), T5, gs)
+    gs, fmt = p["gs"], p["fmt"]
+    w = bqd.pack(to_dev(p["codes"]), fmt, gs)
     with forced_kernel(kernel):
-        y = bqd.qmv(to_dev(p["x"]), w, to_dev(p["scales"]), to_dev(p["biases"]), T5, gs)
+        y = bqd.qmv(to_dev(p["x"]), w, to_dev(p["scales"]), to_dev(p["biases"]), fmt, gs)
     torch.cuda.synchronize()
     assert bqd.device_status() == 0
-    packed = oracle.c_pack(p["codes"], T5, gs)
+    packed = oracle.c_pack(p["codes"], fmt, gs)
     xs = p["x"] if m_rows is None else p["x"][m_rows]
-    yr, bound = oracle.c_qmv_rows(xs, packed, p["scales"], p["biases"], T5, gs, rows=n_rows)
+    yr, bound = oracle.c_qmv_rows(xs, packed, p["scales"], p["biases"], fmt, gs, rows=n_rows)
     yg = y.cpu().numpy().astype(np.float64)
     if m_rows is not None:
         yg = yg[m_rows]
@@ -98,6 +100,110 @@ FULL = [(M, N, K) for M in (32, 512, 2048) for (N, K) in [(17408, 5120), (5120, 
 def test_full_size_sampled(M, N, K):
     rng = np.random.default_rng(M + N)
     p = synth.problem(T5, M, N, K, 128, sym=True)
+    m_rows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, 10)]))
+    n_rows = np.unique(np.concatenate([[0, 127, 128, N - 1], rng.integers(0, N, 12)]))
+    run(p, None, m_rows=m_rows, n_rows=n_rows)
+
+
+# ---- 1/2-bit formats --------------------------------------------------------------
+
+# (M, N, K): K down to one group (gs=128: K=128 is a single K step), ragged M and N
+AFFINE_SMALL = SMALL + [(17, 33, 128), (40, 257, 384)]
+
+
+@pytest.mark.parametrize("fmt", [F1, F2])
+@pytest.mark.parametrize("gs", [64, 128])
+@pytest.mark.parametrize("sym", [False, True])
+def test_affine_small_shapes_all_outputs(fmt, gs, sym):
+    for M, N, K in AFFINE_SMALL:
+        if K % gs:
+            continue
+        run(synth.problem(fmt, M, N, K, gs, sym=sym))
+
+
+@pytest.mark.parametrize("fmt", [F1, F2, T5])
+@pytest.mark.parametrize("gs", [64, 128])
+def test_forced_product_at_decode_sizes(fmt, gs):
+    """BQD_FORCE_KERNEL=qmm runs the product for M <= 16 too (one x tile of 32
+    columns, mostly empty): still exact to the bar."""
+    for M, N, K in [(1, 129, 1024), (5, 256, 2048), (16, 40, 1024)]:
+        run(synth.problem(fmt, M, N, K, gs, sym=fmt == T5), "qmm")
+
+
+@pytest.mark.parametrize("fmt", [F1, F2])
+def test_affine_default_dispatch_takes_the_product_and_agrees(fmt):
+    """M > 16 goes to the product by default (bit-identical to the forced call);
+    the generic CUDA-core kernel, an independent implementation, meets the same bar."""
+    import torch
+    p = synth.problem(fmt, 40, 256, 2048, 64)
+    w = bqd.pack(to_dev(p["codes"]), fmt, 64)
+    x, s, b = to_dev(p["x"]), to_dev(p["scales"]), to_dev(p["biases"])
+    y_default = bqd.qmv(x, w, s, b, fmt, 64)
+    with forced_kernel("qmm"):
+        y_forced = bqd.qmv(x, w, s, b, fmt, 64)
+    with forced_kernel("generic"):
+        y_generic = bqd.qmv(x, w, s, b, fmt, 64)
+    torch.cuda.synchronize()
+    assert torch.equal(y_default.view(torch.int16), y_forced.view(torch.int16))
+    run(p, None)
+    packed = oracle.c_pack(p["codes"], fmt, 64)
+    yr, bound = oracle.c_qmv_rows(p["x"], packed, p["scales"], p["biases"], fmt, 64)
+    assert_within_tolerance(y_generic.cpu().numpy(), yr, bound)
+
+
+@pytest.mark.parametrize("fmt", [F1, F2])
+def test_affine_large_scales_use_the_exact_decode(fmt):
+    """|s| >= 63 would overflow the fp16 constant -1024*s: those groups take the
+    (magic - offset) * s form; both forms give fp16(s*q) exactly."""
+    rng = np.random.default_rng(9)
+    p = synth.problem(fmt, 24, 160, 1024, 64)
+    p["scales"] = (np.abs(rng.normal(0, 200, size=p["scales"].shape)) + 1).astype(np.float16)
+    p["biases"] = (-p["scales"].astype(np.float32) * 0.5).astype(np.float16)
+    p["x"] = (p["x"].astype(np.float32) * 1e-3).astype(np.float16)
+    run(p)
+
+
+@pytest.mark.parametrize("fmt", [F1, F2])
+def test_affine_one_hot_x_recovers_the_weights(fmt):
+    """x = e_k: y[m, n] is the dequantised weight fp16(fp16(s*q) + b) exactly
+    (one non-zero product, accumulated in fp32, rounded once to fp16)."""
+    import torch
+    M, N, K, gs = 32, 200, 512, 64
+    p = synth.problem(fmt, M, N, K, gs)
+    ks = np.arange(M) * 13 % K
+    x = np.zeros((M, K), dtype=np.float16)
+    x[np.arange(M), ks] = 1.0
+    w = bqd.pack(to_dev(p["codes"]), fmt, gs)
+    y = bqd.qmv(to_dev(x), w, to_dev(p["scales"]), to_dev(p["biases"]), fmt, gs)
+    torch.cuda.synchronize()
+    s = p["scales"][:, ks // gs].astype(np.float32)            # [N, M]
+    b = p["biases"][:, ks // gs].astype(np.float32)
+    q = p["codes"][:, ks].astype(np.float32)
+    want = ((s * q).astype(np.float16).astype(np.float32) + b).astype(np.float16).T
+    assert np.array_equal(y.cpu().numpy().view(np.int16), want.view(np.int16))
+
+
+@pytest.mark.parametrize("fmt", [F1, F2])
+def test_affine_zero_codes_zero_bias_give_exact_zeros(fmt):
+    import torch
+    M, N, K, gs = 48, 300, 1024, 128
+    p = synth.problem(fmt, M, N, K, gs)
+    w = bqd.pack(to_dev(np.zeros_like(p["codes"])), fmt, gs)
+    b = torch.zeros((N, K // gs), dtype=torch.float16, device="cuda")
+    y = bqd.qmv(to_dev(p["x"]), w, to_dev(p["scales"]), b, fmt, gs)
+    torch.cuda.synchronize()
+    assert torch.all(y == 0)
+
+
+AFFINE_FULL = [(fmt, M, N, K) for fmt in (F1, F2) for M in (32, 512, 2048)
+               for (N, K) in [(17408, 5120), (5120, 17408)]]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("fmt,M,N,K", AFFINE_FULL)
+def test_affine_full_size_sampled(fmt, M, N, K):
+    rng = np.random.default_rng(M + N + fmt)
+    p = synth.problem(fmt, M, N, K, 128)
     m_rows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, 10)]))
     n_rows = np.unique(np.concatenate([[0, 127, 128, N - 1], rng.integers(0, N, 12)]))
     run(p, None, m_rows=m_rows, n_rows=n_rows)
