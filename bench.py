@@ -14,7 +14,8 @@ weights + fp16 scales + fp16 biases (0 for sym and t5) + fp16 x + fp16 y.
 pinned host memory and results copied back inside the timed region; the
 weights are the model's resident state.  The prefill matrix product is
 timed separately in TFLOP/s: t5 (key "qmm"), 2-bit and 1-bit affine with
-biases (keys "qmm_affine2", "qmm_affine1").
+biases (keys "qmm_affine2", "qmm_affine1").  The speculative-decoding
+verification kernel is timed in GB/s of logits read (key "spec_verify").
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -355,6 +356,37 @@ def time_qmm(dev, fmt: int, reps: int = 10):
     return rows, tot_flop / (tot_ms * 1e-3) / 1e12
 
 
+SPEC_CASE = (64, 8, 151936)  # sequences, draft tokens, vocabulary (a Qwen-sized vocabulary)
+
+
+def time_spec_verify(dev, reps: int = 20):
+    """Speculative-decoding verification over fp16 logits [B, D+1, V]: GB/s of
+    logits read (plus drafts and results) per call; two logits sets of 175 MB
+    alternate, each larger than the L2."""
+    import torch
+    import bit_quantized_decode_unpack_gb300 as bqd
+    B, D, V = SPEC_CASE
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    sets = [torch.randn((B, D + 1, V), generator=gen, device=dev).to(torch.float16) for _ in range(2)]
+    draft = torch.randint(0, V, (B, D), generator=gen, device=dev, dtype=torch.int32)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    for i in range(3):
+        bqd.spec_decode_verify(sets[i % 2], draft, acc, nxt)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(reps):
+        bqd.spec_decode_verify(sets[i % 2], draft, acc, nxt)
+    e1.record()
+    e1.synchronize()
+    us = e0.elapsed_time(e1) / reps * 1e3
+    nbytes = B * (D + 1) * V * 2 + B * D * 4 + 2 * B * 4
+    del sets
+    return us, nbytes / (us * 1e-6) / 1e9
+
+
 def kernel_traffic_from_profiles():
     """DRAM-bytes / algorithmic-bytes ratio of the QMV kernels from the committed
     ncu summaries, or None when a kernel source changed since it was taken."""
@@ -496,12 +528,22 @@ def main():
     ap.add_argument("--table", type=str, default=None, help="write the per-call table (CSV) here")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-qmm", action="store_true", help="skip the prefill matrix-product timings")
+    ap.add_argument("--no-spec", action="store_true", help="skip the speculative-decoding verification timing")
     ap.add_argument("--cpu-rows", type=int, default=0, help="0: sized for ~12 s of oracle work")
     ap.add_argument("--case", type=str, default=None, help="fmt,M,N,K,gs[,sym]: time one configuration")
+    ap.add_argument("--spec-case", type=str, default=None,
+                    help="B,D,V: time the speculative-decoding verification on fp16 logits")
     args = ap.parse_args()
 
     if args.case:
         return run_case(args.case, args.sets)
+    if args.spec_case:
+        import torch
+        global SPEC_CASE
+        SPEC_CASE = tuple(int(v) for v in args.spec_case.split(","))
+        us, gbs = time_spec_verify(torch.device("cuda", 0))
+        print(json.dumps({"spec_case": args.spec_case, "us_per_call": us, "gbs": gbs}), flush=True)
+        return 0
 
     if args.impl == "reference":
         return reference_arm(args)
@@ -582,6 +624,15 @@ def main():
                              "roofline": {"bound": "tensor", "achieved": qagg, "peak": tf_peak, "unit": "TFLOP/s",
                                           "frac": qagg / tf_peak,
                                           "peak_source": src + " bf16 burst (fp16 runs at the bf16 rate)"}}
+        if not args.no_spec:
+            us, gbs = time_spec_verify(dev)
+            hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+            B, D, V = SPEC_CASE
+            line["spec_verify"] = {"metric": "speculative-decoding verification GB/s (fp16 logits read)",
+                                   "value": gbs, "unit": "GB/s", "us_per_call": us,
+                                   "config": {"sequences": B, "draft_tokens": D, "vocab": V, "dtype": "f16"},
+                                   "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                                "frac": gbs / hbm, "peak_source": src}}
         if not args.no_cpu_baseline:
             import oracle
             oracle.build()

@@ -21,6 +21,8 @@ FMT_AFFINE1 = 1
 FMT_AFFINE2 = 2
 FMT_T5 = 3
 FORMATS = {"affine1": FMT_AFFINE1, "affine2": FMT_AFFINE2, "t5": FMT_T5}
+DTYPE_F16 = 1
+DTYPE_F32 = 2
 
 BQD_OK = 0
 ABI_VERSION = 1  # must match BQD_ABI_VERSION in include/bqd.h
@@ -69,6 +71,8 @@ def load() -> ctypes.CDLL:
         lib.bqd_validate_t5.restype = i32
         lib.bqd_detect_sym.argtypes = [vp, vp, i64, i64, ctypes.c_float, vp, vp]
         lib.bqd_detect_sym.restype = i32
+        lib.bqd_spec_decode_verify.argtypes = [vp, i32, vp, i64, i64, i64, vp, vp, vp, vp]
+        lib.bqd_spec_decode_verify.restype = i32
         lib.bqd_device_status.argtypes = [vp]
         lib.bqd_device_status.restype = i32
         if lib.bqd_abi_version() != ABI_VERSION:
@@ -194,6 +198,32 @@ def detect_sym(scales, biases, ratio: float, out=None, stream=None):
     _check("bqd_detect_sym", load().bqd_detect_sym(_ptr(scales), _ptr(biases), N, G, float(ratio),
                                                    _ptr(out), _stream(stream)))
     return out
+
+
+def spec_decode_verify(logits, draft, accepted=None, next_token=None, argmax_out=None, stream=None):
+    """Greedy speculative-decoding verification (bqd_spec_decode_verify).
+
+    logits fp16|fp32 [B, D+1, V], draft int32 [B, D] (device).  Returns
+    (accepted int32 [B], next_token int32 [B]); pass ``argmax_out`` (int32
+    [B, D+1]) to also receive every row's argmax."""
+    import torch
+    B, D1, V = logits.shape
+    if logits.dtype == torch.float16:
+        dt = DTYPE_F16
+    elif logits.dtype == torch.float32:
+        dt = DTYPE_F32
+    else:
+        raise TypeError(f"logits must be float16 or float32, got {logits.dtype}")
+    if draft.dtype != torch.int32 or tuple(draft.shape) != (B, D1 - 1):
+        raise ValueError(f"draft must be int32 [{B}, {D1 - 1}], got {draft.dtype} {tuple(draft.shape)}")
+    if accepted is None:
+        accepted = torch.empty((B,), dtype=torch.int32, device=logits.device)
+    if next_token is None:
+        next_token = torch.empty((B,), dtype=torch.int32, device=logits.device)
+    _check("bqd_spec_decode_verify", load().bqd_spec_decode_verify(
+        _ptr(logits), dt, _ptr(draft) if D1 > 1 else None, B, D1 - 1, V, _ptr(accepted), _ptr(next_token),
+        _ptr(argmax_out), _stream(stream)))
+    return accepted, next_token
 
 
 def device_status(stream=None) -> int:

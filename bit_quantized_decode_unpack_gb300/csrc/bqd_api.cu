@@ -141,6 +141,22 @@ extern "C" int bqd_qmv_sym(const void *x, const void *w_packed, const void *scal
     return qmv_common(x, w_packed, scales, nullptr, ratio, M, N, K, format, group_size, out, stream);
 }
 
+extern "C" int bqd_spec_decode_verify(const void *logits, int dtype, const int32_t *draft, int64_t B, int64_t D,
+                                      int64_t V, int32_t *accepted, int32_t *next_token, int32_t *argmax_out,
+                                      bqd_stream_t stream)
+{
+    if (dtype != BQD_DTYPE_F16 && dtype != BQD_DTYPE_F32) return BQD_ERR_INVALID_ARG;
+    if (B < 0 || B > ((int64_t)1 << 26) || D < 0 || D > 4095 || V < 1 || V > ((int64_t)1 << 31) - 1024)
+        return BQD_ERR_INVALID_ARG;
+    if (B == 0) return BQD_OK;
+    if (!logits || !accepted || !next_token || (D > 0 && !draft)) return BQD_ERR_INVALID_ARG;
+    if (!aligned(logits, dtype == BQD_DTYPE_F16 ? 2 : 4) || !aligned(accepted, 4) || !aligned(next_token, 4) ||
+        (draft && !aligned(draft, 4)) || (argmax_out && !aligned(argmax_out, 4)))
+        return BQD_ERR_ALIGNMENT;
+    return launch_spec_decode_verify(logits, dtype, draft, B, D, V, accepted, next_token, argmax_out,
+                                     reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" int bqd_pack(const uint8_t *codes, int64_t N, int64_t K, int format, int group_size,
                         void *w_packed, bqd_stream_t stream)
 {

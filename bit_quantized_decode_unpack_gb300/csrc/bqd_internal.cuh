@@ -48,6 +48,10 @@ int launch_qmv_t5(const QmvArgs &a, cudaStream_t s);
 // format (16-byte aligned weight base; t5 rows a multiple of 16 bytes).
 int launch_qmm(const QmvArgs &a, cudaStream_t s);
 
+// Speculative-decoding verification (validated arguments, B >= 1).
+int launch_spec_decode_verify(const void *logits, int dtype, const int32_t *draft, int64_t B, int64_t D, int64_t V,
+                              int32_t *accepted, int32_t *next_token, int32_t *argmax_out, cudaStream_t s);
+
 int launch_pack(const uint8_t *codes, int64_t N, int64_t K, int fmt, int gs,
                 uint8_t *w, cudaStream_t s);
 int launch_unpack(const uint8_t *w, int64_t N, int64_t K, int fmt, int gs,

@@ -1,6 +1,7 @@
 /*
  * bqd.h -- C ABI of libbqd: the decode-time low-bit quantized matrix-vector
- * product (QMV) and its t5 prefill matrix product (QMM) on GB300 (sm_103a).
+ * product (QMV), its prefill matrix product (QMM) and the speculative-decoding
+ * verification kernel, on GB300 (sm_103a).
  *
  * Page defining the operations: "oMLX Bonsai 自定义内核:Qwen 系列快速 QMV 路径
  * 完整解析" (oMLX Bonsai custom kernels: the fast QMV path for the Qwen
@@ -66,6 +67,9 @@ enum {
 
 /* weight formats */
 enum { BQD_FMT_AFFINE1 = 1, BQD_FMT_AFFINE2 = 2, BQD_FMT_T5 = 3 };
+
+/* element types of bqd_spec_decode_verify's logits */
+enum { BQD_DTYPE_F16 = 1, BQD_DTYPE_F32 = 2 };
 
 /* opaque CUDA stream (binary-compatible with cudaStream_t / CUstream) */
 typedef struct CUstream_st *bqd_stream_t;
@@ -166,6 +170,33 @@ int bqd_validate_t5(const uint8_t *w_t5, int64_t N, int64_t K, int group_size,
  */
 int bqd_detect_sym(const void *scales, const void *biases, int64_t N, int64_t G,
                    float ratio, int *d_mismatches, bqd_stream_t stream);
+
+/*
+ * Speculative-decoding verification in one kernel (§三: spec_decode_verify
+ * fuses "compare the draft tokens -> count the accepted length -> produce the
+ * correction token").  The page gives no formula; greedy reading:
+ *   t[b, i]       = argmax over v of logits[b, i, v], i = 0 .. D (ties: the
+ *                   smallest v; NaN entries are never chosen; a row of NaNs
+ *                   gives -1)
+ *   accepted[b]   = the largest a in [0, D] with draft[b, i] == t[b, i] for
+ *                   every i < a (a -1 from a row of NaNs matches nothing)
+ *   next_token[b] = t[b, accepted[b]]: the target's token where the draft was
+ *                   first rejected, or the bonus token after D accepted drafts
+ * Arguments (device pointers):
+ *   logits      [B, D+1, V] of `dtype` (BQD_DTYPE_F16 or BQD_DTYPE_F32),
+ *               aligned to its element size; row (b, i) scores the token
+ *               that follows the prefix and draft[b, 0 .. i-1]
+ *   draft       int32 [B, D] (may be NULL when D == 0); ids outside [0, V)
+ *               never match
+ *   accepted, next_token  int32 [B]
+ *   argmax_out  int32 [B, D+1], or NULL: t[b, i] of every row
+ * Sizes: 0 <= B <= 2^26, 0 <= D <= 4095, 1 <= V <= 2^31 - 1024.  B == 0
+ * launches nothing.  Every logit is read once (the call is bound by HBM
+ * bandwidth); one thread-block cluster of min(D+1, 16) CTAs per sequence.
+ */
+int bqd_spec_decode_verify(const void *logits, int dtype, const int32_t *draft, int64_t B, int64_t D,
+                           int64_t V, int32_t *accepted, int32_t *next_token, int32_t *argmax_out,
+                           bqd_stream_t stream);
 
 /*
  * Device-side failure report.  Kernels that wait on asynchronous copies

@@ -10,6 +10,9 @@ Two independent implementations of the same definitions:
 * ``bqd_oracle.c`` (C99, one weight at a time; loaded through ctypes here),
 * ``oracle.py`` (NumPy, whole-matrix array operations).
 
+``spec_verify.py`` holds the oracle of the speculative-decoding verification
+step (plain Python loops).
+
 Parity pins: every function here is checked in ``tests/test_oracle_pins.py``
 against closed forms, exhaustive enumerations and brute force.  None of them
 is "parity unpinned".
@@ -25,6 +28,7 @@ from pathlib import Path
 import numpy as np
 
 from . import oracle as np_oracle  # noqa: F401  (the NumPy twin)
+from .spec_verify import spec_decode_verify  # noqa: F401  (speculative-decoding verification)
 from .oracle import (DEFAULT_SYM_RATIO, FMT_AFFINE1, FMT_AFFINE2, FMT_T5,  # noqa: F401
                      FORMATS, GROUP_SIZES, MAX_CODE, t5_bytes_per_group)
 
