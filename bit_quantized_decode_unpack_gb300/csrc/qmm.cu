@@ -354,6 +354,13 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
 #pragma unroll
         for (int d = 0; d < NPAT; ++d)
             mgx[d] = ((magic(plo(d)) & 0xFFFFu) | (magic(phi(d)) & 0xFFFF0000u)) ^ p.zero;
+        // this thread's 16-byte chunks of the A tile, relative to the stage
+        uint32_t a_off[GS / 16];
+#pragma unroll
+        for (int q = 0; q < GS / 16; ++q) {
+            const int chunk = (GS / 16) * h + q;
+            a_off[q] = (uint32_t)((chunk >> 3) * 16384) + sw128_offset(r, chunk & 7);
+        }
         if (steps > 0) fetch(g_lo);
         for (int it = 0; it < steps; ++it) {
             const int s = it % NST;
@@ -479,15 +486,14 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
                     }
             }
             // store into the stage's A tile (K-major, 128-byte swizzle): 16-byte
-            // chunk q of this half is chunk (GS/16) h + q of the row
-            uint8_t *at = smem + (size_t)s * stage_bytes;
+            // chunk q of this half is chunk (GS/16) h + q of the row.  Rows past
+            // N decode to zeros: their bytes, scale and bias were loaded as 0.
+            const uint32_t at = smem_addr(smem + (size_t)s * stage_bytes);
 #pragma unroll
-            for (int q = 0; q < GS / 16; ++q) {
-                const int chunk = (GS / 16) * h + q;
-                uint4 v = make_uint4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
-                if (!rok) v = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(at + (chunk >> 3) * 16384 + sw128_offset(r, chunk & 7)) = v;
-            }
+            for (int q = 0; q < GS / 16; ++q)
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(at + a_off[q]), "r"(hv[4 * q]),
+                             "r"(hv[4 * q + 1]), "r"(hv[4 * q + 2]), "r"(hv[4 * q + 3])
+                             : "memory");
             fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
             mbar_arrive(smem_addr(&a_full[s]));
         }
