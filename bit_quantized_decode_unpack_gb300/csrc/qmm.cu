@@ -246,10 +246,10 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
     if (warp == kTmaWarpQ) {
         // ---- X producer ---------------------------------------------------------
         if (lane == 0) {
-            int issued = 0;
+            int issued = 0, s = 0;
+            uint32_t rpar = 1;  // parity of empty_bar[s] that frees it for step it (>= NST)
             for (int it = 0; it < steps; ++it) {
-                const int s = it % NST;
-                if (it >= NST && !wait_bounded(smem_addr(&empty_bar[s]), ((it / NST) - 1) & 1)) {
+                if (it >= NST && !wait_bounded(smem_addr(&empty_bar[s]), rpar)) {
                     abort_flag = 1;
                     break;
                 }
@@ -260,6 +260,10 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
                 for (int sub = 0; sub < NSUB; ++sub)
                     tma_load_2d(smem_addr(xt + sub * p.bx * 128), &xmap, k + 64 * sub, m0, bar);
                 issued = it + 1;
+                if (++s == NST) {
+                    s = 0;
+                    rpar ^= 1u;
+                }
             }
             if (abort_flag) {
                 // drain the copies this CTA issued (bounded) before anyone leaves
@@ -272,9 +276,9 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
         if (lane == 0) {
             const uint32_t idesc = idesc_f16(128, p.bx);
             bool ok = true;
+            int s = 0;
+            uint32_t par = 0;
             for (int it = 0; it < steps; ++it) {
-                const int s = it % NST;
-                const uint32_t par = (it / NST) & 1;
                 ok = wait_bounded(smem_addr(&x_full[s]), par) && wait_bounded(smem_addr(&a_full[s]), par);
                 if (!ok) break;
                 tc_fence_after();
@@ -288,6 +292,10 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
                     tc_mma(tmem, ad, bd, idesc, (it > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(smem_addr(&empty_bar[s]));
+                if (++s == NST) {
+                    s = 0;
+                    par ^= 1u;
+                }
             }
             if (!ok) abort_flag = 1;
             tc_commit(smem_addr(&done_bar));  // arrives once every issued MMA has completed
@@ -318,17 +326,23 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
         uint32_t an[T5F ? 1 : HW];
         uint16_t sb_n = 0, bb_n = 0;
         // the next K step's bytes, scale and bias are requested before the
-        // current one is decoded
-        auto fetch = [&](int g) {
+        // current one is decoded; steps are fetched in order, so the sources
+        // advance by one group per call
+        long long t5_start = (long long)g_lo * B + fb;
+        const uint8_t *wp = wrow + (long long)g_lo * (2 * HB) + h * HB;
+        const __half *sp = srow + g_lo, *bp = brow ? brow + g_lo : nullptr;
+        auto fetch = [&]() {
             if constexpr (T5F) {
-                const long long start = (long long)g * B + fb;
+                const long long start = t5_start;
+                t5_start += B;
                 const long long astart = start & ~15LL;
                 ow_n = (int)(start & 15);
                 w0n = rok ? *reinterpret_cast<const uint4 *>(wrow + astart) : make_uint4(0, 0, 0, 0);
                 w1n = rok && astart + 16 < p.row_bytes ? *reinterpret_cast<const uint4 *>(wrow + astart + 16)
                                                        : make_uint4(0, 0, 0, 0);
             } else {
-                const uint8_t *src = wrow + (long long)g * (2 * HB) + h * HB;
+                const uint8_t *src = wp;
+                wp += 2 * HB;
                 if constexpr (HW == 4) {
                     const uint4 v = rok ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0, 0, 0, 0);
                     an[0] = v.x; an[1] = v.y; an[2] = v.z; an[3] = v.w;
@@ -339,8 +353,10 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
                     an[0] = rok ? *reinterpret_cast<const uint32_t *>(src) : 0u;
                 }
             }
-            sb_n = rok ? __half_as_ushort(srow[g]) : (uint16_t)0;
-            bb_n = rok && brow ? __half_as_ushort(brow[g]) : (uint16_t)0;
+            sb_n = rok ? __half_as_ushort(*sp) : (uint16_t)0;
+            bb_n = rok && bp ? __half_as_ushort(*bp) : (uint16_t)0;
+            ++sp;
+            if (bp) ++bp;
         };
         // magic exponents: t5 fields sit at bits 2d of both halves; 1/2-bit
         // pair d has its low code at mantissa bit PLO(d), its high one at PHI(d)
@@ -361,9 +377,10 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
             const int chunk = (GS / 16) * h + q;
             a_off[q] = (uint32_t)((chunk >> 3) * 16384) + sw128_offset(r, chunk & 7);
         }
-        if (steps > 0) fetch(g_lo);
+        if (steps > 0) fetch();
+        int s = 0;          // stage of step it
+        uint32_t rpar = 1;  // parity of empty_bar[s] that frees it for step it (>= NST)
         for (int it = 0; it < steps; ++it) {
-            const int s = it % NST;
             uint32_t cur[HW];
             if constexpr (T5F) {
                 const uint32_t W[8] = {w0n.x, w0n.y, w0n.z, w0n.w, w1n.x, w1n.y, w1n.z, w1n.w};
@@ -384,8 +401,8 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
             const uint16_t sb = sb_n;
             const uint16_t bb = rok ? (brow ? bb_n : __half_as_ushort(sym_bias(__ushort_as_half(sb), p.ratio)))
                                     : (uint16_t)0;
-            if (it + 1 < steps) fetch(g_lo + it + 1);
-            if (it >= NST && !wait_bounded(smem_addr(&empty_bar[s]), ((it / NST) - 1) & 1)) {
+            if (it + 1 < steps) fetch();
+            if (it >= NST && !wait_bounded(smem_addr(&empty_bar[s]), rpar)) {
                 abort_flag = 1;
                 break;
             }
@@ -496,6 +513,10 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
                              : "memory");
             fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
             mbar_arrive(smem_addr(&a_full[s]));
+            if (++s == NST) {
+                s = 0;
+                rpar ^= 1u;
+            }
         }
     }
 
