@@ -316,9 +316,24 @@ QMM_CASES = [(M, N, K) for M in (32, 512, 2048) for (N, K) in [(17408, 5120), (5
 
 
 def time_qmm(dev, fmt: int, reps: int = 10):
-    """Prefill matrix product (M > 16 -> tcgen05 kernel) of one format, gs=128:
-    TFLOP/s per case (2*M*N*K flops).  Each case rotates through enough weight
-    sets (codes, scales, biases for 1/2-bit) to exceed the 129 MB L2."""
+    """The tcgen05 prefill matrix product of one format, gs=128: TFLOP/s per
+    case (2*M*N*K flops).  The product is forced (BQD_FORCE_KERNEL=qmm) so that
+    each case times that kernel, whatever the dispatcher would pick at that M.
+    Each case rotates through enough weight sets (codes, scales, biases for
+    1/2-bit) to exceed the 129 MB L2."""
+    import os
+    old = os.environ.get("BQD_FORCE_KERNEL")
+    os.environ["BQD_FORCE_KERNEL"] = "qmm"
+    try:
+        return _time_qmm(dev, fmt, reps)
+    finally:
+        if old is None:
+            os.environ.pop("BQD_FORCE_KERNEL", None)
+        else:
+            os.environ["BQD_FORCE_KERNEL"] = old
+
+
+def _time_qmm(dev, fmt: int, reps: int):
     import torch
     import bit_quantized_decode_unpack_gb300 as bqd
     from bit_quantized_decode_unpack_gb300 import synth

@@ -26,8 +26,9 @@ int sm_count()
 // Testing override of the dispatcher: BQD_FORCE_KERNEL=generic|mma|tma|qmm
 // (read on every call so that a test can compare the kernels in one process).
 // "mma" forces the register-streaming tensor-core kernels (the prefill
-// product for M > 16), "tma" the TMA-ring decode kernels, "qmm" the tcgen05
-// prefill product at any M; a forced kernel's "unsupported" is returned as is.
+// product for M > 16), "tma" the TMA-ring decode kernels at any M, "qmm" the
+// tcgen05 prefill product at any M; a forced kernel's "unsupported" is
+// returned as is.
 static int forced_kernel()
 {
     const char *v = getenv("BQD_FORCE_KERNEL");
@@ -104,8 +105,15 @@ static int qmv_common(const void *x, const void *w, const void *scales, const vo
 
     const int force = forced_kernel();
     if (force != 1) {
-        // prefill (M > 16): fused unpack + tcgen05 matrix product
-        if (M > 16 || force == 4) {
+        // prefill: fused unpack + tcgen05 matrix product.  Below these sizes the
+        // decode kernels (all passes of their x rows in one launch) are faster
+        // (measured on a 27B-class layer): the product's 128-row tiles need a
+        // wide N (gate/up: 136 tiles; down: 40) to fill the GPU at small M,
+        // and the t5 decode kernel takes 5 rows per pass against 8 for 1/2-bit
+        const bool wide = N >= 8192;
+        const bool prefill = format == BQD_FMT_T5 ? (wide ? M > 10 : M > 15)
+                                                  : (wide ? M > (format == BQD_FMT_AFFINE2 ? 16 : 32) : M > 64);
+        if ((prefill && force != 3) || force == 4) {
             int st = launch_qmm(a, s);
             if (st != BQD_ERR_UNSUPPORTED || force == 2 || force == 4) return st;
         }

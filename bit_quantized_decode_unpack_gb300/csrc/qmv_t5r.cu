@@ -63,7 +63,9 @@ struct T5RParams {
     const __half *biases;
     __half *out;
     float ratio;
-    int M, N, K, G, chunks, S, Cs, stages, RS;
+    int M;     // x rows per pass (the staging and fragment layouts)
+    int Mtot;  // x rows of the call; pass blockIdx.y takes rows M*y .. M*y+M-1
+    int N, K, G, chunks, S, Cs, stages, RS;
     uint32_t stage_bytes;
     uint32_t zero;  // always 0: keeps the magic constants opaque (in registers)
 };
@@ -246,7 +248,8 @@ __global__ void __launch_bounds__(kThreadsR, 2)
                 const int k0 = (c_lo + it) * kCodesR;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    tma_2d(xraw_a + (uint32_t)(it & 1) * XB + (uint32_t)(j * 512 * M), &xmap, k0 + 256 * j, 0, bar);
+                    tma_2d(xraw_a + (uint32_t)(it & 1) * XB + (uint32_t)(j * 512 * M), &xmap, k0 + 256 * j,
+                           M * (int)blockIdx.y, bar);
             }
         };
         const int pre = min(NST, ncl);
@@ -497,11 +500,13 @@ __global__ void __launch_bounds__(kThreadsR, 2)
     for (int q = 0; q < 4; ++q) v[q] = (acc[0][q] + acc[1][q]) + (acc[2][q] + acc[3][q]);
 
     // ---- results: value q is row r0 + 8 (q >> 1), column 2t + (q & 1) -------------------
+    const int Mv = min(M, p.Mtot - M * (int)blockIdx.y);  // rows of this pass that exist
+    __half *outg = p.out + (size_t)(M * blockIdx.y) * p.N;
     if (S == 1) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int n = n0 + r0 + 8 * (q >> 1), m = 2 * t + (q & 1);
-            if (n < p.N && m < M) p.out[(size_t)m * p.N + n] = __float2half_rn(v[q]);
+            if (n < p.N && m < Mv) outg[(size_t)m * p.N + n] = __float2half_rn(v[q]);
         }
         return;
     }
@@ -522,7 +527,7 @@ __global__ void __launch_bounds__(kThreadsR, 2)
         float sum = 0.f;
         for (int k = 0; k < S; ++k) sum += red[((size_t)k * RS + lr) * 8 + m];
         const int n = n0 + row0 + lr;
-        if (n < p.N) p.out[(size_t)m * p.N + n] = __float2half_rn(sum);
+        if (n < p.N && m < Mv) outg[(size_t)m * p.N + n] = __float2half_rn(sum);
     }
 }
 
@@ -603,8 +608,9 @@ int cluster_slots_r(int S, size_t smem)
     return slots;
 }
 
+// P passes of x rows run side by side in one launch (grid rows)
 template <int GS, bool HAS_BIAS>
-bool plan_r(int M, int N, int chunks, RPlan &best)
+bool plan_r(int M, int N, int chunks, int P, RPlan &best)
 {
     const int R = (N + kRowsR - 1) / kRowsR;
     const int sms = sm_count();
@@ -624,7 +630,7 @@ bool plan_r(int M, int N, int chunks, RPlan &best)
         const size_t sm = t5r_smem<GS, HAS_BIAS>(M, S, st, RS);
         const int slots = S == 1 ? 2 * sms : cluster_slots_r<GS, HAS_BIAS>(S, sm);
         if (slots <= 0) continue;
-        const int waves = (R + slots - 1) / slots;
+        const int waves = (R * P + slots - 1) / slots;
         // time ~ waves x (chunks per CTA + first-stage latency and reduction,
         // ~1 chunk); a single-stage ring (no overlap of copy and compute) costs
         // about twice as much per chunk
@@ -643,7 +649,8 @@ template <int GS, bool HAS_BIAS>
 int launch_r(const T5RParams &p0, const CUtensorMap &wmap, cudaStream_t s)
 {
     RPlan pl;
-    if (!plan_r<GS, HAS_BIAS>(p0.M, p0.N, p0.chunks, pl)) return BQD_ERR_UNSUPPORTED;
+    const int P = (p0.Mtot + p0.M - 1) / p0.M;
+    if (!plan_r<GS, HAS_BIAS>(p0.M, p0.N, p0.chunks, P, pl)) return BQD_ERR_UNSUPPORTED;
     T5RParams p = p0;
     p.S = pl.S;
     p.Cs = pl.Cs;
@@ -656,12 +663,13 @@ int launch_r(const T5RParams &p0, const CUtensorMap &wmap, cudaStream_t s)
     bmap = smap;
     if (HAS_BIAS && !encode_2d(bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.biases, p.G, p.N, (int64_t)p.G * 2, GPC))
         return BQD_ERR_CUDA;
-    // x of this pass: [M][K] fp16, box {256 codes, M rows}
+    // x: [Mtot][K] fp16, box {256 codes, M rows}; a pass's rows past Mtot read as zeros
     CUtensorMap xmap;
-    if (!encode_2d(xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.x, p.K, p.M, (int64_t)p.K * 2, 256, p.M)) return BQD_ERR_CUDA;
+    if (!encode_2d(xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.x, p.K, p.Mtot, (int64_t)p.K * 2, 256, p.M))
+        return BQD_ERR_CUDA;
     if (getenv("BQD_DEBUG_PLAN"))
-        fprintf(stderr, "bqd t5r plan: N=%d K=%d M=%d gs=%d -> S=%d Cs=%d stages=%d R=%d grid=%d smem=%zu\n", p.N, p.K,
-                p.M, GS, pl.S, pl.Cs, pl.stages, pl.R, pl.R * pl.S, pl.smem);
+        fprintf(stderr, "bqd t5r plan: N=%d K=%d M=%d (%d per pass) gs=%d -> S=%d Cs=%d stages=%d R=%d grid=%dx%d smem=%zu\n",
+                p.N, p.K, p.Mtot, p.M, GS, pl.S, pl.Cs, pl.stages, pl.R, pl.R * pl.S, P, pl.smem);
     auto kern = qmv_t5r_kernel<GS, HAS_BIAS>;
     static int configured_dev[64] = {0};
     int dev = 0;
@@ -673,7 +681,7 @@ int launch_r(const T5RParams &p0, const CUtensorMap &wmap, cudaStream_t s)
         configured_dev[dev] = 1;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(pl.R * pl.S);
+    cfg.gridDim = dim3(pl.R * pl.S, P);
     cfg.blockDim = dim3(kThreadsR);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = s;
@@ -726,16 +734,16 @@ int launch_qmv_t5r(const QmvArgs &a, cudaStream_t s)
     p.S = p.Cs = p.stages = p.RS = 0;
     p.stage_bytes = 0;
     const bool hb = a.biases != nullptr;
-    for (int64_t m0 = 0; m0 < a.M; m0 += kMaxMR) {
-        p.M = (int)((a.M - m0) < kMaxMR ? (a.M - m0) : kMaxMR);
-        p.x = a.x + m0 * a.K;
-        p.out = a.out + m0 * a.N;
-        int st;
-        if (a.gs == 64) st = hb ? launch_r<64, true>(p, wmap, s) : launch_r<64, false>(p, wmap, s);
-        else st = hb ? launch_r<128, true>(p, wmap, s) : launch_r<128, false>(p, wmap, s);
-        if (st != BQD_OK) return st;
-    }
-    return BQD_OK;
+    // passes of at most kMaxMR x rows, all in one launch (grid row y = rows
+    // kMaxMR*y ..): the fixed cost of a call is paid once and later passes find
+    // the weights in L2
+    if (a.M > (int64_t)kMaxMR * 65535) return BQD_ERR_UNSUPPORTED;
+    p.M = (int)(a.M < kMaxMR ? a.M : kMaxMR);
+    p.Mtot = (int)a.M;
+    p.x = a.x;
+    p.out = a.out;
+    if (a.gs == 64) return hb ? launch_r<64, true>(p, wmap, s) : launch_r<64, false>(p, wmap, s);
+    return hb ? launch_r<128, true>(p, wmap, s) : launch_r<128, false>(p, wmap, s);
 }
 
 }  // namespace bqd

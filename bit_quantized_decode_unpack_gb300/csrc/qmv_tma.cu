@@ -317,6 +317,10 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     const int S = p.S;
     const int rank = S > 1 ? (int)cluster_ctarank() : 0;
     const int n0 = (blockIdx.x / S) * kRowsC;
+    // pass blockIdx.y takes x rows 8y .. 8y+7 (M > 8 runs every pass in this one launch)
+    const int M = min(8, p.M - 8 * (int)blockIdx.y);
+    const __half *xg = p.x + (size_t)(8 * blockIdx.y) * p.K;
+    __half *outg = p.out + (size_t)(8 * blockIdx.y) * p.N;
     const int c_lo = rank * p.Cs;
     const int ncl = max(0, min(p.Cs, p.chunks - c_lo));
     const int NST = p.stages;
@@ -370,7 +374,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
 #pragma unroll
             for (int m = 0; m < MP; ++m) {
                 xv[m] = make_uint4(0, 0, 0, 0);
-                if (m < p.M) xv[m] = ld_x16(p.x + (size_t)m * p.K + (size_t)(c_lo + it) * kChunkT + 8 * lane);
+                if (m < M) xv[m] = ld_x16(xg + (size_t)m * p.K + (size_t)(c_lo + it) * kChunkT + 8 * lane);
             }
         };
         uint32_t Az[NPR];
@@ -612,7 +616,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int n = n0 + rb + 16 * tl + 8 * (q >> 1), m = 2 * t + (q & 1);
-                if (n < p.N && m < p.M) p.out[(size_t)m * p.N + n] = __float2half_rn(acc[tl][q]);
+                if (n < p.N && m < M) outg[(size_t)m * p.N + n] = __float2half_rn(acc[tl][q]);
             }
         return;
     }
@@ -632,12 +636,12 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
     const int row0 = rank * RS;
     const int nrow = min(RS, kRowsC - row0);
-    for (int e = tid; e < nrow * p.M; e += kCons * 32) {
-        const int lr = e / p.M, m = e % p.M;
+    for (int e = tid; e < nrow * M; e += kCons * 32) {
+        const int lr = e / M, m = e % M;
         float v = 0.f;
         for (int k = 0; k < S; ++k) v += red[((size_t)k * RS + lr) * 8 + m];
         const int n = n0 + row0 + lr;
-        if (n < p.N) p.out[(size_t)m * p.N + n] = __float2half_rn(v);
+        if (n < p.N) outg[(size_t)m * p.N + n] = __float2half_rn(v);
     }
 }
 
@@ -705,8 +709,9 @@ int cluster_slots_t(int S, size_t smem)
     return slots;
 }
 
+// P passes of x rows run side by side in one launch (grid rows)
 template <int FMT, int GS, bool HAS_BIAS, int MP>
-bool plan_t(int N, int chunks, TPlan &best)
+bool plan_t(int N, int chunks, int P, TPlan &best)
 {
     constexpr int GPC = kChunkT / GS;
     const int R = (N + kRowsC - 1) / kRowsC;
@@ -732,7 +737,7 @@ bool plan_t(int N, int chunks, TPlan &best)
         const size_t sm = tma_smem<FMT, GS, HAS_BIAS, MP>(S, st, RS, BX);
         const int slots = S == 1 ? 2 * sms : cluster_slots_t<FMT, GS, HAS_BIAS, MP>(S, sm);
         if (slots <= 0) continue;
-        const int waves = (R + slots - 1) / slots;
+        const int waves = (R * P + slots - 1) / slots;
         // time ~ waves x (chunks per CTA + first-stage latency and reduction, ~2 chunks)
         const double cost = (double)waves * (Cs + 2) + 0.1 * S;
         if (cost < best_cost - 1e-9) {
@@ -762,7 +767,8 @@ template <int FMT, int GS, bool HAS_BIAS, int MP>
 int launch_t(const TmaParams &p0, const CUtensorMap &map, int chunks, cudaStream_t s)
 {
     TPlan pl;
-    if (!plan_t<FMT, GS, HAS_BIAS, MP>(p0.N, chunks, pl)) return BQD_ERR_UNSUPPORTED;
+    const int P = (p0.M + 7) / 8;
+    if (!plan_t<FMT, GS, HAS_BIAS, MP>(p0.N, chunks, P, pl)) return BQD_ERR_UNSUPPORTED;
     TmaParams p = p0;
     p.S = pl.S;
     p.Cs = pl.Cs;
@@ -774,8 +780,8 @@ int launch_t(const TmaParams &p0, const CUtensorMap &map, int chunks, cudaStream
     bmap = smap;
     if (HAS_BIAS && !encode_f16(bmap, p.biases, p.G, p.N, pl.BX)) return BQD_ERR_CUDA;
     if (getenv("BQD_DEBUG_PLAN"))
-        fprintf(stderr, "bqd tma plan: N=%d K=%d M=%d gs=%d -> S=%d Cs=%d stages=%d R=%d BX=%d grid=%d smem=%zu\n", p.N,
-                p.K, p.M, GS, pl.S, pl.Cs, pl.stages, pl.R, pl.BX, pl.R * pl.S, pl.smem);
+        fprintf(stderr, "bqd tma plan: N=%d K=%d M=%d gs=%d -> S=%d Cs=%d stages=%d R=%d BX=%d grid=%dx%d smem=%zu\n",
+                p.N, p.K, p.M, GS, pl.S, pl.Cs, pl.stages, pl.R, pl.BX, pl.R * pl.S, P, pl.smem);
     auto kern = qmv_tma_kernel<FMT, GS, HAS_BIAS, MP>;
     static int configured_dev[64] = {0};
     int dev = 0;
@@ -787,7 +793,7 @@ int launch_t(const TmaParams &p0, const CUtensorMap &map, int chunks, cudaStream
         configured_dev[dev] = 1;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(pl.R * pl.S);
+    cfg.gridDim = dim3(pl.R * pl.S, P);
     cfg.blockDim = dim3(kThreadsT);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = s;
@@ -858,22 +864,19 @@ int launch_qmv_tma(const QmvArgs &a, cudaStream_t s)
     p.zero = 0;
     p.S = p.Cs = p.stages = p.RS = 0;
     const bool hb = a.biases != nullptr;
-    for (int64_t m0 = 0; m0 < a.M; m0 += 8) {
-        const int M = (int)((a.M - m0) < 8 ? (a.M - m0) : 8);
-        const int MP = M <= 4 ? 4 : 8;
-        p.M = M;
-        p.x = a.x + m0 * a.K;
-        p.out = a.out + m0 * a.N;
-        int st;
-        if (b64)
-            st = a.gs == 64 ? launch_fmt_gs<BQD_FMT_AFFINE2, 64>(p, map, p.chunks, hb, MP, s)
-                            : launch_fmt_gs<BQD_FMT_AFFINE2, 128>(p, map, p.chunks, hb, MP, s);
-        else
-            st = a.gs == 64 ? launch_fmt_gs<BQD_FMT_AFFINE1, 64>(p, map, p.chunks, hb, MP, s)
-                            : launch_fmt_gs<BQD_FMT_AFFINE1, 128>(p, map, p.chunks, hb, MP, s);
-        if (st != BQD_OK) return st;
-    }
-    return BQD_OK;
+    // M <= 8: one pass with 4 or 8 B-fragment columns; larger M: passes of 8
+    // x rows, all in one launch (grid row y = rows 8y .. 8y+7), so that the
+    // fixed cost of a call is paid once and later passes find the weights in L2
+    if (a.M > (int64_t)8 * 65535) return BQD_ERR_UNSUPPORTED;
+    const int MP = a.M <= 4 ? 4 : 8;
+    p.M = (int)a.M;
+    p.x = a.x;
+    p.out = a.out;
+    if (b64)
+        return a.gs == 64 ? launch_fmt_gs<BQD_FMT_AFFINE2, 64>(p, map, p.chunks, hb, MP, s)
+                          : launch_fmt_gs<BQD_FMT_AFFINE2, 128>(p, map, p.chunks, hb, MP, s);
+    return a.gs == 64 ? launch_fmt_gs<BQD_FMT_AFFINE1, 64>(p, map, p.chunks, hb, MP, s)
+                      : launch_fmt_gs<BQD_FMT_AFFINE1, 128>(p, map, p.chunks, hb, MP, s);
 }
 
 }  // namespace bqd

@@ -1,5 +1,7 @@
-"""GPU parity of the prefill matrix product (tcgen05 tensor cores, M > 16)
-against the float64 oracle, through the C ABI: t5 and the 1/2-bit formats.
+"""GPU parity of the prefill matrix product (tcgen05 tensor cores; the
+dispatcher's choice for large M) against the float64 oracle, through the C
+ABI: t5 and the 1/2-bit formats.  Most cases force the product
+(BQD_FORCE_KERNEL=qmm) so that it is tested at every shape.
 
 Page: "oMLX Bonsai 自定义内核:Qwen 系列快速 QMV 路径完整解析" §二.3 -- for M > 16
 the t5 weights go through a fused unpack + matrix-multiply kernel; §二.1 -- the
@@ -19,7 +21,7 @@ pytestmark = pytest.mark.gpu
 T5, F1, F2 = bqd.FMT_T5, bqd.FMT_AFFINE1, bqd.FMT_AFFINE2
 
 
-def run(p, kernel="mma", m_rows=None, n_rows=None):
+def run(p, kernel="qmm", m_rows=None, n_rows=None):
     import torch
     gs, fmt = p["gs"], p["fmt"]
     w = bqd.pack(to_dev(p["codes"]), fmt, gs)
@@ -132,10 +134,11 @@ def test_forced_product_at_decode_sizes(fmt, gs):
 
 @pytest.mark.parametrize("fmt", [F1, F2])
 def test_affine_default_dispatch_takes_the_product_and_agrees(fmt):
-    """M > 16 goes to the product by default (bit-identical to the forced call);
-    the generic CUDA-core kernel, an independent implementation, meets the same bar."""
+    """A prefill-sized M (here 70 rows of a narrow layer) goes to the product by
+    default (bit-identical to the forced call); the generic CUDA-core kernel,
+    an independent implementation, meets the same bar."""
     import torch
-    p = synth.problem(fmt, 40, 256, 2048, 64)
+    p = synth.problem(fmt, 70, 256, 2048, 64)
     w = bqd.pack(to_dev(p["codes"]), fmt, 64)
     x, s, b = to_dev(p["x"]), to_dev(p["scales"]), to_dev(p["biases"])
     y_default = bqd.qmv(x, w, s, b, fmt, 64)
@@ -174,7 +177,8 @@ def test_affine_one_hot_x_recovers_the_weights(fmt):
     x = np.zeros((M, K), dtype=np.float16)
     x[np.arange(M), ks] = 1.0
     w = bqd.pack(to_dev(p["codes"]), fmt, gs)
-    y = bqd.qmv(to_dev(x), w, to_dev(p["scales"]), to_dev(p["biases"]), fmt, gs)
+    with forced_kernel("qmm"):  # the product materialises the fp16 weights
+        y = bqd.qmv(to_dev(x), w, to_dev(p["scales"]), to_dev(p["biases"]), fmt, gs)
     torch.cuda.synchronize()
     s = p["scales"][:, ks // gs].astype(np.float32)            # [N, M]
     b = p["biases"][:, ks // gs].astype(np.float32)
@@ -190,7 +194,8 @@ def test_affine_zero_codes_zero_bias_give_exact_zeros(fmt):
     p = synth.problem(fmt, M, N, K, gs)
     w = bqd.pack(to_dev(np.zeros_like(p["codes"])), fmt, gs)
     b = torch.zeros((N, K // gs), dtype=torch.float16, device="cuda")
-    y = bqd.qmv(to_dev(p["x"]), w, to_dev(p["scales"]), b, fmt, gs)
+    with forced_kernel("qmm"):
+        y = bqd.qmv(to_dev(p["x"]), w, to_dev(p["scales"]), b, fmt, gs)
     torch.cuda.synchronize()
     assert torch.all(y == 0)
 
@@ -206,4 +211,4 @@ def test_affine_full_size_sampled(fmt, M, N, K):
     p = synth.problem(fmt, M, N, K, 128)
     m_rows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, 10)]))
     n_rows = np.unique(np.concatenate([[0, 127, 128, N - 1], rng.integers(0, N, 12)]))
-    run(p, None, m_rows=m_rows, n_rows=n_rows)
+    run(p, "qmm", m_rows=m_rows, n_rows=n_rows)

@@ -78,10 +78,11 @@ def test_tensor_core_paths_forced(kernel, fmt, gs, sym):
 
 # TMA-ring kernel: its envelope is K a multiple of 256 with K/gs a multiple of
 # 8 (16-byte scale rows); shapes span row blocks of 256 with ragged tails,
-# split-K clusters of many sizes (portable and not), M up to 8 and two passes
-# for M > 8
+# split-K clusters of many sizes (portable and not), M up to 8 in one pass and
+# passes of 8 rows (grid rows of one launch) beyond, the last one ragged
 TMA_SHAPES = [(1, 1, 1024), (2, 127, 1024), (3, 256, 2048), (4, 257, 3072), (5, 383, 4096), (7, 1024, 5120),
-              (8, 2000, 1024), (9, 200, 2048), (16, 130, 1024), (1, 5120, 17408), (5, 300, 17408), (2, 4096, 6144)]
+              (8, 2000, 1024), (9, 200, 2048), (16, 130, 1024), (1, 5120, 17408), (5, 300, 17408), (2, 4096, 6144),
+              (27, 300, 2048)]
 
 
 @pytest.mark.parametrize("fmt", [F1, F2])
@@ -95,9 +96,10 @@ def test_tma_kernel_shapes(fmt, gs, sym):
 
 
 # t5 TMA-ring kernel: K a multiple of 1024; ragged 128-row blocks, split-K
-# clusters, passes of at most 6 x rows (M = 7, 12, 16 take several)
+# clusters, passes of at most 5 x rows (grid rows of one launch; M = 6, 7, 12,
+# 16, 23 take several, the last one ragged)
 T5R_SHAPES = [(1, 1, 1024), (2, 127, 1024), (3, 129, 2048), (4, 300, 3072), (5, 1000, 5120), (6, 383, 4096),
-              (7, 260, 2048), (12, 64, 1024), (16, 130, 2048), (1, 5120, 17408), (5, 200, 17408)]
+              (7, 260, 2048), (12, 64, 1024), (16, 130, 2048), (1, 5120, 17408), (5, 200, 17408), (23, 129, 2048)]
 
 
 @pytest.mark.parametrize("gs", [64, 128])
