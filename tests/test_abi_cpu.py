@@ -121,3 +121,32 @@ def test_other_entry_points_validate_on_host(lib):
 def test_binding_names_match_the_c_abi():
     for name in _declared_symbols():
         assert hasattr(bqd, name[len("bqd_"):]), name
+
+
+def test_spec_decode_verify_validates_on_host(lib):
+    """bqd_spec_decode_verify rejects bad arguments before any launch (no GPU
+    is touched for these), and B == 0 is a no-op."""
+    INV, ALIGN = 1, 3
+    vp = ctypes.c_void_p
+    f = lib.bqd_spec_decode_verify
+    ok = dict(lg=0x1000, dt=1, dr=0x2000, B=2, D=3, V=100, a=0x3000, n=0x4000, am=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        p = lambda v: None if v is None else vp(v)
+        return f(p(a["lg"]), a["dt"], p(a["dr"]), a["B"], a["D"], a["V"], p(a["a"]), p(a["n"]), p(a["am"]), None)
+
+    assert call(dt=3) == INV               # unknown logits type
+    assert call(B=-1) == INV
+    assert call(D=-1) == INV
+    assert call(D=4096) == INV             # above the documented maximum
+    assert call(V=0) == INV
+    assert call(V=(1 << 31)) == INV
+    assert call(lg=None) == INV
+    assert call(a=None) == INV
+    assert call(n=None) == INV
+    assert call(dr=None) == INV            # drafts are needed when D > 0
+    assert call(lg=0x1001) == ALIGN        # fp16 logits need 2-byte alignment
+    assert call(lg=0x1002, dt=2) == ALIGN  # fp32 logits need 4-byte alignment
+    assert call(a=0x3002) == ALIGN
+    assert call(B=0, lg=None, dr=None, a=None, n=None) == 0
