@@ -184,13 +184,21 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c)
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-template <int FMT, int GS>
+// NH = 2: the CTA owns two 256-column blocks of x (two N=256 accumulators,
+// all 512 TMEM columns), so each decoded weight tile serves 512 columns; its
+// K step is then 64 codes (half a 128-group), which keeps two stages of
+// [A 16 KB | X 64 KB] in shared memory.  1/2-bit only (t5 groups are not
+// byte-aligned at 32-code boundaries).
+template <int FMT, int GS, int NH>
 __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParams &p)
 {
     constexpr bool T5F = FMT == BQD_FMT_T5;
+    static_assert(NH == 1 || (!T5F && NH == 2), "two column blocks per CTA: 1/2-bit only");
+    constexpr int KS = NH == 2 ? 64 : GS;  // codes per K step
+    constexpr int SPG = GS / KS;           // K steps per group (1 or 2)
     constexpr int B = GS == 64 ? 13 : 26;  // t5 bytes per group
-    constexpr int NSUB = GS / 64;          // 64-code sub-tiles per K step
-    constexpr int A_BYTES = 128 * GS * 2;  // A tile per stage
+    constexpr int NSUB = KS / 64;          // 64-code sub-tiles per K step
+    constexpr int A_BYTES = 128 * KS * 2;  // A tile per stage
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t x_full[kMaxStagesQ], a_full[kMaxStagesQ], empty_bar[kMaxStagesQ], done_bar;
     __shared__ uint32_t tmem_base;
@@ -204,12 +212,13 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
     const int tile = blockIdx.x / S;
     const int n_tiles = (p.N + 127) / 128;
     const int nt = tile % n_tiles, mt = tile / n_tiles;
-    const int n0 = nt * 128, m0 = mt * p.bx;
+    const int C = NH * p.bx;  // x columns of the CTA
+    const int n0 = nt * 128, m0 = mt * C;
     const int g_lo = rank * p.gpr;
     const int g_hi = min(p.G, g_lo + p.gpr);
-    const int steps = max(0, g_hi - g_lo);
+    const int steps = max(0, g_hi - g_lo) * SPG;
     const int NST = p.stages;
-    const uint32_t X_BYTES = (uint32_t)p.bx * GS * 2;
+    const uint32_t X_BYTES = (uint32_t)C * KS * 2;
 
     // 1024-byte aligned stage ring: [A tile | X tile] per stage
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -235,7 +244,7 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
         mbar_init(smem_addr(&done_bar), 1);
         abort_flag = 0;
     }
-    if (warp == kMmaWarpQ) tmem_alloc(smem_addr(&tmem_base), (uint32_t)p.bx);
+    if (warp == kMmaWarpQ) tmem_alloc(smem_addr(&tmem_base), (uint32_t)C);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -255,10 +264,13 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
                 }
                 const uint32_t bar = smem_addr(&x_full[s]);
                 mbar_arrive_expect_tx(bar, X_BYTES);
-                const int k = (g_lo + it) * GS;
+                const int k = g_lo * GS + it * KS;
                 uint8_t *xt = smem + (size_t)s * stage_bytes + A_BYTES;
-                for (int sub = 0; sub < NSUB; ++sub)
-                    tma_load_2d(smem_addr(xt + sub * p.bx * 128), &xmap, k + 64 * sub, m0, bar);
+                // column block hh, sub-tile sub: [bx rows][64 codes] at (hh NSUB + sub) bx 128 bytes
+                for (int hh = 0; hh < NH; ++hh)
+                    for (int sub = 0; sub < NSUB; ++sub)
+                        tma_load_2d(smem_addr(xt + (hh * NSUB + sub) * p.bx * 128), &xmap, k + 64 * sub,
+                                    m0 + hh * p.bx, bar);
                 issued = it + 1;
                 if (++s == NST) {
                     s = 0;
@@ -285,11 +297,14 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
                 const uint32_t a0 = smem_addr(smem + (size_t)s * stage_bytes);
                 const uint32_t x0 = a0 + A_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < GS / 16; ++kk) {
+                for (int kk = 0; kk < KS / 16; ++kk) {
                     const int sub = kk >> 2, within = kk & 3;
                     const uint64_t ad = sw128_desc(a0 + sub * 16384 + within * 32);
-                    const uint64_t bd = sw128_desc(x0 + sub * p.bx * 128 + within * 32);
-                    tc_mma(tmem, ad, bd, idesc, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int hh = 0; hh < NH; ++hh) {
+                        const uint64_t bd = sw128_desc(x0 + (hh * NSUB + sub) * p.bx * 128 + within * 32);
+                        tc_mma(tmem + (uint32_t)(hh * p.bx), ad, bd, idesc, (it > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
                 tc_commit(smem_addr(&empty_bar[s]));
                 if (++s == NST) {
@@ -315,10 +330,11 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
         // loads (row_bytes is a multiple of 16 here) and realigned in registers.
         constexpr int FB1 = GS == 128 ? 12 : 6;
         constexpr int NWH = GS == 128 ? 4 : 2;
-        // 1/2-bit: the half group is HB bytes (HW words) at byte g*2HB + h*HB,
-        // one aligned load (row_bytes = G * 2HB and the base is 16-byte aligned)
+        // 1/2-bit: half h of a K step is HB bytes (HW words) at byte
+        // (first code of the step)/CPB + h*HB, one aligned load (row_bytes is
+        // a multiple of 2HB and the base is 16-byte aligned)
         constexpr int CPB = FMT == BQD_FMT_AFFINE2 ? 4 : 8;  // codes per byte
-        constexpr int HB = GS / (2 * CPB);                   // 4, 8 or 16
+        constexpr int HB = KS / (2 * CPB);                   // 4, 8 or 16
         constexpr int HW = T5F ? NWH : HB / 4;               // words decoded per step
         const int fb = h ? FB1 : 0;
         uint4 w0n = make_uint4(0, 0, 0, 0), w1n = make_uint4(0, 0, 0, 0);
@@ -329,8 +345,9 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
         // current one is decoded; steps are fetched in order, so the sources
         // advance by one group per call
         long long t5_start = (long long)g_lo * B + fb;
-        const uint8_t *wp = wrow + (long long)g_lo * (2 * HB) + h * HB;
+        const uint8_t *wp = wrow + (long long)g_lo * (GS / CPB) + h * HB;
         const __half *sp = srow + g_lo, *bp = brow ? brow + g_lo : nullptr;
+        int sstep = 0;  // K steps fetched in the current group (SPG per group)
         auto fetch = [&]() {
             if constexpr (T5F) {
                 const long long start = t5_start;
@@ -355,8 +372,11 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
             }
             sb_n = rok ? __half_as_ushort(*sp) : (uint16_t)0;
             bb_n = rok && bp ? __half_as_ushort(*bp) : (uint16_t)0;
-            ++sp;
-            if (bp) ++bp;
+            if (++sstep == SPG) {
+                sstep = 0;
+                ++sp;
+                if (bp) ++bp;
+            }
         };
         // magic exponents: t5 fields sit at bits 2d of both halves; 1/2-bit
         // pair d has its low code at mantissa bit PLO(d), its high one at PHI(d)
@@ -371,10 +391,10 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
         for (int d = 0; d < NPAT; ++d)
             mgx[d] = ((magic(plo(d)) & 0xFFFFu) | (magic(phi(d)) & 0xFFFF0000u)) ^ p.zero;
         // this thread's 16-byte chunks of the A tile, relative to the stage
-        uint32_t a_off[GS / 16];
+        uint32_t a_off[KS / 16];
 #pragma unroll
-        for (int q = 0; q < GS / 16; ++q) {
-            const int chunk = (GS / 16) * h + q;
+        for (int q = 0; q < KS / 16; ++q) {
+            const int chunk = (KS / 16) * h + q;
             a_off[q] = (uint32_t)((chunk >> 3) * 16384) + sw128_offset(r, chunk & 7);
         }
         if (steps > 0) fetch();
@@ -410,9 +430,9 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
             // constants -2^(10-p)*s stay finite for |s| < 63; else the exact
             // (magic - offset) * s form is used
             const bool fast = fabsf(__half2float(__ushort_as_half(sb))) < 63.f;
-            // this thread's GS/4 words (GS/2 codes, two per word: code 2i low,
-            // 2i+1 high): half h of the group
-            uint32_t hv[GS / 4];
+            // this thread's KS/4 words (KS/2 codes, two per word: code 2i low,
+            // 2i+1 high): half h of the K step
+            uint32_t hv[KS / 4];
             if constexpr (T5F) {
                 uint32_t c[5];
 #pragma unroll
@@ -503,11 +523,11 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
                     }
             }
             // store into the stage's A tile (K-major, 128-byte swizzle): 16-byte
-            // chunk q of this half is chunk (GS/16) h + q of the row.  Rows past
+            // chunk q of this half is chunk (KS/16) h + q of the row.  Rows past
             // N decode to zeros: their bytes, scale and bias were loaded as 0.
             const uint32_t at = smem_addr(smem + (size_t)s * stage_bytes);
 #pragma unroll
-            for (int q = 0; q < GS / 16; ++q)
+            for (int q = 0; q < KS / 16; ++q)
                 asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(at + a_off[q]), "r"(hv[4 * q]),
                              "r"(hv[4 * q + 1]), "r"(hv[4 * q + 2]), "r"(hv[4 * q + 3])
                              : "memory");
@@ -533,14 +553,14 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
     const int r = q4 * 32 + lane;
     const int row = n0 + r;
     // columns of this warp: half (warp >> 2) of bx, in blocks of 32 (bx = 32: warps 0-3 only)
-    const int cw = p.bx >= 64 ? p.bx / 2 : p.bx;
-    const int c_beg = p.bx >= 64 ? (warp >> 2) * cw : 0;
-    const bool drains = warp < kDecodeWarpsQ && (p.bx >= 64 || warp < 4);
+    const int cw = C >= 64 ? C / 2 : C;
+    const int c_beg = C >= 64 ? (warp >> 2) * cw : 0;
+    const bool drains = warp < kDecodeWarpsQ && (C >= 64 || warp < 4);
     if (drains && S > 1 && rank != 0 && steps > 0) {
         for (int c0 = c_beg; c0 < c_beg + cw; c0 += 32) {
             uint32_t v[32];
             tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)c0, v);
-            float *dst = red + ((size_t)(rank - 1) * 128 + r) * p.bx + c0;
+            float *dst = red + ((size_t)(rank - 1) * 128 + r) * C + c0;
 #pragma unroll
             for (int q = 0; q < 32; ++q) st_cluster_f32(smem_addr(dst + q), 0, __uint_as_float(v[q]));
         }
@@ -559,7 +579,7 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
             for (int q = 0; q < 32; ++q) {
                 float acc = __uint_as_float(v[q]);
                 for (int rr = 1; rr < S; ++rr)
-                    if (rr * p.gpr < p.G) acc += red[((size_t)(rr - 1) * 128 + r) * p.bx + c0 + q];
+                    if (rr * p.gpr < p.G) acc += red[((size_t)(rr - 1) * 128 + r) * C + c0 + q];
                 const int m = m0 + c0 + q;
                 if (row < p.N && m < p.M) p.out[(size_t)m * p.N + row] = __float2half_rn(acc);
             }
@@ -567,21 +587,21 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarpQ) tmem_dealloc(tmem, (uint32_t)p.bx);
+    if (warp == kMmaWarpQ) tmem_dealloc(tmem, (uint32_t)C);
 }
 
 template <int GS>
 __global__ void __launch_bounds__(kThreadsQ, 1)
 qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
 {
-    qmm_body<BQD_FMT_T5, GS>(xmap, p);
+    qmm_body<BQD_FMT_T5, GS, 1>(xmap, p);
 }
 
-template <int FMT, int GS>
+template <int FMT, int GS, int NH>
 __global__ void __launch_bounds__(kThreadsQ, 1)
 qmm_affine_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
 {
-    qmm_body<FMT, GS>(xmap, p);
+    qmm_body<FMT, GS, NH>(xmap, p);
 }
 
 // ---- host side -------------------------------------------------------------------
@@ -601,14 +621,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-template <int FMT, int GS>
+template <int FMT, int GS, int NH>
 int launch_gs(const QmmParams &p, const CUtensorMap &map, int tiles, size_t smem, cudaStream_t s)
 {
     void (*kern)(const CUtensorMap, const QmmParams);
     if constexpr (FMT == BQD_FMT_T5)
         kern = qmm_t5_kernel<GS>;
     else
-        kern = qmm_affine_kernel<FMT, GS>;
+        kern = qmm_affine_kernel<FMT, GS, NH>;
     static int configured_dev[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -666,10 +686,18 @@ int launch_qmm(const QmvArgs &a, cudaStream_t s)
     p.row_bytes = a.row_bytes;
     p.zero = 0;
     p.bx = a.M <= 32 ? 32 : (a.M <= 64 ? 64 : (a.M <= 128 ? 128 : 256));
-    const int n_tiles = (p.N + 127) / 128, m_tiles = (p.M + p.bx - 1) / p.bx;
+    // 1/2-bit with more than 256 x rows on a wide layer: two 256-column blocks
+    // per CTA (the decoded weight tile serves 512 columns), K steps of 64
+    // codes.  Narrow layers keep one block: their few 128-row tiles would
+    // leave SMs idle (measured: down projection, M=512, 813 -> 470 TFLOP/s)
+    const bool pair = a.fmt != BQD_FMT_T5 && a.M > 256 && a.N >= 8192;
+    const int NH = pair ? 2 : 1;
+    const int KS = pair ? 64 : a.gs;
+    const int cols = NH * p.bx;
+    const int n_tiles = (p.N + 127) / 128, m_tiles = (p.M + cols - 1) / cols;
     const int tiles = n_tiles * m_tiles;
     const int sms = sm_count();
-    const size_t per_stage = (size_t)128 * a.gs * 2 + (size_t)p.bx * a.gs * 2;
+    const size_t per_stage = (size_t)128 * KS * 2 + (size_t)cols * KS * 2;
     p.stages = (int)((kQmmSmemMax - 1024) / per_stage);
     if (p.stages > kMaxStagesQ) p.stages = kMaxStagesQ;
     if (p.stages < 2) return BQD_ERR_UNSUPPORTED;
@@ -677,7 +705,7 @@ int launch_qmm(const QmvArgs &a, cudaStream_t s)
     // rank keeps >= 4 groups, and the (S-1) fp32 partial tiles fit the ring
     int S = 1;
     while (S < 8 && tiles * (S + 1) <= sms && p.G >= 4 * (S + 1) &&
-           (size_t)S * 128 * p.bx * 4 <= (size_t)p.stages * per_stage)
+           (size_t)S * 128 * cols * 4 <= (size_t)p.stages * per_stage)
         ++S;
     p.S = S;
     p.gpr = (p.G + S - 1) / S;
@@ -693,16 +721,23 @@ int launch_qmm(const QmvArgs &a, cudaStream_t s)
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return BQD_ERR_CUDA;
     if (getenv("BQD_DEBUG_PLAN"))
-        fprintf(stderr, "bqd qmm plan: fmt=%d M=%d N=%d K=%d gs=%d -> bx=%d tiles=%d S=%d gpr=%d stages=%d smem=%zu\n",
-                a.fmt, p.M, p.N, p.K, a.gs, p.bx, tiles, S, p.gpr, p.stages, smem);
+        fprintf(stderr, "bqd qmm plan: fmt=%d M=%d N=%d K=%d gs=%d -> bx=%d x%d tiles=%d S=%d gpr=%d stages=%d smem=%zu\n",
+                a.fmt, p.M, p.N, p.K, a.gs, p.bx, NH, tiles, S, p.gpr, p.stages, smem);
     if (a.fmt == BQD_FMT_T5)
-        return a.gs == 64 ? launch_gs<BQD_FMT_T5, 64>(p, map, tiles, smem, s)
-                          : launch_gs<BQD_FMT_T5, 128>(p, map, tiles, smem, s);
-    if (a.fmt == BQD_FMT_AFFINE2)
-        return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE2, 64>(p, map, tiles, smem, s)
-                          : launch_gs<BQD_FMT_AFFINE2, 128>(p, map, tiles, smem, s);
-    return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE1, 64>(p, map, tiles, smem, s)
-                      : launch_gs<BQD_FMT_AFFINE1, 128>(p, map, tiles, smem, s);
+        return a.gs == 64 ? launch_gs<BQD_FMT_T5, 64, 1>(p, map, tiles, smem, s)
+                          : launch_gs<BQD_FMT_T5, 128, 1>(p, map, tiles, smem, s);
+    if (a.fmt == BQD_FMT_AFFINE2) {
+        if (pair)
+            return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE2, 64, 2>(p, map, tiles, smem, s)
+                              : launch_gs<BQD_FMT_AFFINE2, 128, 2>(p, map, tiles, smem, s);
+        return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE2, 64, 1>(p, map, tiles, smem, s)
+                          : launch_gs<BQD_FMT_AFFINE2, 128, 1>(p, map, tiles, smem, s);
+    }
+    if (pair)
+        return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE1, 64, 2>(p, map, tiles, smem, s)
+                          : launch_gs<BQD_FMT_AFFINE1, 128, 2>(p, map, tiles, smem, s);
+    return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE1, 64, 1>(p, map, tiles, smem, s)
+                      : launch_gs<BQD_FMT_AFFINE1, 128, 1>(p, map, tiles, smem, s);
 }
 
 }  // namespace bqd

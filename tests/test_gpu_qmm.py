@@ -109,8 +109,9 @@ def test_full_size_sampled(M, N, K):
 
 # ---- 1/2-bit formats --------------------------------------------------------------
 
-# (M, N, K): K down to one group (gs=128: K=128 is a single K step), ragged M and N
-AFFINE_SMALL = SMALL + [(17, 33, 128), (40, 257, 384)]
+# (M, N, K): K down to one group (gs=128: K=128 is a single K step), ragged M
+# and N
+AFFINE_SMALL = SMALL + [(17, 33, 128), (40, 257, 384), (300, 257, 1024), (260, 40, 128)]
 
 
 @pytest.mark.parametrize("fmt", [F1, F2])
@@ -121,6 +122,24 @@ def test_affine_small_shapes_all_outputs(fmt, gs, sym):
         if K % gs:
             continue
         run(synth.problem(fmt, M, N, K, gs, sym=sym))
+
+
+@pytest.mark.parametrize("fmt", [F1, F2])
+@pytest.mark.parametrize("gs", [64, 128])
+@pytest.mark.parametrize("sym", [False, True])
+def test_affine_two_column_blocks_per_cta(fmt, gs, sym):
+    """M > 256 on a wide layer (N >= 8192): each CTA owns two 256-column x
+    blocks (two TMEM accumulators) with 64-code K steps.  M = 300 leaves one
+    block half empty, 513 adds a nearly empty CTA column; N = 8200 a ragged
+    row tile.  Sampled outputs (rows of the first, a middle and the last tile)."""
+    rng = np.random.default_rng(fmt * 10 + gs)
+    for M, N, K in [(300, 8200, 256), (513, 8192, 384)]:
+        if K % gs:
+            continue
+        p = synth.problem(fmt, M, N, K, gs, sym=sym)
+        m_rows = np.unique(np.concatenate([[0, 255, 256, M - 1], rng.integers(0, M, 12)]))
+        n_rows = np.unique(np.concatenate([[0, 127, 4096, N - 1], rng.integers(0, N, 12)]))
+        run(p, m_rows=m_rows, n_rows=n_rows)
 
 
 @pytest.mark.parametrize("fmt", [F1, F2, T5])
