@@ -372,7 +372,10 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
             }
             sb_n = rok ? __half_as_ushort(*sp) : (uint16_t)0;
             bb_n = rok && bp ? __half_as_ushort(*bp) : (uint16_t)0;
-            if (++sstep == SPG) {
+            if constexpr (SPG == 1) {
+                ++sp;
+                if (bp) ++bp;
+            } else if (++sstep == SPG) {
                 sstep = 0;
                 ++sp;
                 if (bp) ++bp;
