@@ -400,34 +400,14 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
             const int chunk = (KS / 16) * h + q;
             a_off[q] = (uint32_t)((chunk >> 3) * 16384) + sw128_offset(r, chunk & 7);
         }
-        if (steps > 0) fetch();
         int s = 0;          // stage of step it
         uint32_t rpar = 1;  // parity of empty_bar[s] that frees it for step it (>= NST)
-        for (int it = 0; it < steps; ++it) {
-            uint32_t cur[HW];
-            if constexpr (T5F) {
-                const uint32_t W[8] = {w0n.x, w0n.y, w0n.z, w0n.w, w1n.x, w1n.y, w1n.z, w1n.w};
-                const int wo = ow_n >> 2, sh = (ow_n & 3) * 8;
-                uint32_t V[NWH + 1];
-#pragma unroll
-                for (int i = 0; i <= NWH; ++i) {
-                    const uint32_t lo = (wo & 1) ? W[i + 1] : W[i];
-                    const uint32_t hi = (wo & 1) ? W[i + 3] : W[i + 2];
-                    V[i] = (wo & 2) ? hi : lo;
-                }
-#pragma unroll
-                for (int q = 0; q < NWH; ++q) cur[q] = __funnelshift_r(V[q], V[q + 1], sh);
-            } else {
-#pragma unroll
-                for (int q = 0; q < HW; ++q) cur[q] = an[q];
-            }
-            const uint16_t sb = sb_n;
-            const uint16_t bb = rok ? (brow ? bb_n : __half_as_ushort(sym_bias(__ushort_as_half(sb), p.ratio)))
-                                    : (uint16_t)0;
-            if (it + 1 < steps) fetch();
+        // one K step after its data is in registers: wait for the stage, decode,
+        // store the A tile, arrive; false once a bounded wait has expired
+        auto step_body = [&](int it, const uint32_t (&cur)[HW], uint16_t sb, uint16_t bb) -> bool {
             if (it >= NST && !wait_bounded(smem_addr(&empty_bar[s]), rpar)) {
                 abort_flag = 1;
-                break;
+                return false;
             }
             const uint32_t s2 = dup_half(sb), b2 = dup_half(bb);
             // constants -2^(10-p)*s stay finite for |s| < 63; else the exact
@@ -539,6 +519,88 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
             if (++s == NST) {
                 s = 0;
                 rpar ^= 1u;
+            }
+            return true;
+        };
+        if constexpr (NH == 2) {
+            // 64-code steps are short: two steps of bytes, scale and bias are in
+            // flight per thread, in two register slots used alternately (two
+            // steps per iteration, so the slot of each load is a constant).
+            // Loads are unconditional: past the last step the sources stop
+            // advancing and the extra fetch re-reads it (valid memory, unused).
+            uint32_t anq[2][HW];
+            uint16_t sbq[2], bbq[2];
+            int fetched = 0;
+            auto fetch_into = [&](auto U) {
+                constexpr int u = decltype(U)::value;
+                const bool adv = ++fetched < steps;
+                const uint8_t *src = wp;
+                wp += adv ? 2 * HB : 0;
+                if constexpr (HW == 2) {
+                    const uint2 v = rok ? *reinterpret_cast<const uint2 *>(src) : make_uint2(0, 0);
+                    anq[u][0] = v.x;
+                    anq[u][1] = v.y;
+                } else {
+                    anq[u][0] = rok ? *reinterpret_cast<const uint32_t *>(src) : 0u;
+                }
+                sbq[u] = rok ? __half_as_ushort(*sp) : (uint16_t)0;
+                bbq[u] = rok && bp ? __half_as_ushort(*bp) : (uint16_t)0;
+                int gadv = adv ? 1 : 0;
+                if constexpr (SPG > 1) {
+                    sstep += gadv;
+                    gadv = sstep == SPG ? 1 : 0;
+                    sstep = gadv ? 0 : sstep;
+                }
+                sp += gadv;
+                if (bp) bp += gadv;
+            };
+            if (steps > 0) {
+                fetch_into(std::integral_constant<int, 0>{});
+                fetch_into(std::integral_constant<int, 1>{});
+            }
+            bool stop = false;
+            for (int it0 = 0; it0 < steps && !stop; it0 += 2) {
+                auto one = [&](auto U) {
+                    constexpr int u = decltype(U)::value;
+                    const int it = it0 + u;
+                    if (stop || it >= steps) return;
+                    uint32_t cur[HW];
+#pragma unroll
+                    for (int q = 0; q < HW; ++q) cur[q] = anq[u][q];
+                    const uint16_t sb = sbq[u];
+                    const uint16_t bb =
+                        rok ? (brow ? bbq[u] : __half_as_ushort(sym_bias(__ushort_as_half(sb), p.ratio))) : (uint16_t)0;
+                    fetch_into(U);
+                    if (!step_body(it, cur, sb, bb)) stop = true;
+                };
+                one(std::integral_constant<int, 0>{});
+                one(std::integral_constant<int, 1>{});
+            }
+        } else {
+            if (steps > 0) fetch();
+            for (int it = 0; it < steps; ++it) {
+                uint32_t cur[HW];
+                if constexpr (T5F) {
+                    const uint32_t W[8] = {w0n.x, w0n.y, w0n.z, w0n.w, w1n.x, w1n.y, w1n.z, w1n.w};
+                    const int wo = ow_n >> 2, sh = (ow_n & 3) * 8;
+                    uint32_t V[NWH + 1];
+#pragma unroll
+                    for (int i = 0; i <= NWH; ++i) {
+                        const uint32_t lo = (wo & 1) ? W[i + 1] : W[i];
+                        const uint32_t hi = (wo & 1) ? W[i + 3] : W[i + 2];
+                        V[i] = (wo & 2) ? hi : lo;
+                    }
+#pragma unroll
+                    for (int q = 0; q < NWH; ++q) cur[q] = __funnelshift_r(V[q], V[q + 1], sh);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < HW; ++q) cur[q] = an[q];
+                }
+                const uint16_t sb = sb_n;
+                const uint16_t bb = rok ? (brow ? bb_n : __half_as_ushort(sym_bias(__ushort_as_half(sb), p.ratio)))
+                                        : (uint16_t)0;
+                if (it + 1 < steps) fetch();
+                if (!step_body(it, cur, sb, bb)) break;
             }
         }
     }
