@@ -96,7 +96,10 @@ size_t bqd_packed_bytes(int format, int64_t N, int64_t K, int group_size);
  * Quantized matrix-vector / matrix product, §二.1 (M = 1, qmv_fast),
  * §二.2 (M = 2..5, qmv_wide: each packed weight byte is read once for all M
  * rows; sym variant with biases == NULL reads no bias tensor), §二.3 (t5
- * decode, and the fused unpack + tensor-core matrix product for M > 16).
+ * decode, and the fused unpack + tensor-core matrix product for prefill).
+ * Any M >= 0 is accepted; the library picks the kernel (decode kernels for
+ * small M, the fused product once M is large enough for it on the layer's
+ * shape -- beyond 10 to 64 rows depending on format and N).
  *   x        device fp16 [M, K], 16-byte aligned
  *   w_packed device, layout above, 16-byte aligned
  *   scales   device fp16 [N, G], 2-byte aligned
