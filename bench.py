@@ -376,8 +376,10 @@ SPEC_CASE = (64, 8, 151936)  # sequences, draft tokens, vocabulary (a Qwen-sized
 
 def time_spec_verify(dev, reps: int = 20):
     """Speculative-decoding verification over fp16 logits [B, D+1, V]: GB/s of
-    logits read (plus drafts and results) per call; two logits sets of 175 MB
-    alternate, each larger than the L2."""
+    logits read (plus drafts and results) per call.  A CUDA graph of `reps`
+    calls alternating two logits sets (each larger than the L2 at the default
+    size) is replayed, so that small batches time the device, not the host's
+    launch path."""
     import torch
     import bit_quantized_decode_unpack_gb300 as bqd
     B, D, V = SPEC_CASE
@@ -387,18 +389,26 @@ def time_spec_verify(dev, reps: int = 20):
     draft = torch.randint(0, V, (B, D), generator=gen, device=dev, dtype=torch.int32)
     acc = torch.empty(B, dtype=torch.int32, device=dev)
     nxt = torch.empty(B, dtype=torch.int32, device=dev)
-    for i in range(3):
-        bqd.spec_decode_verify(sets[i % 2], draft, acc, nxt)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(reps):
-        bqd.spec_decode_verify(sets[i % 2], draft, acc, nxt)
-    e1.record()
-    e1.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            bqd.spec_decode_verify(sets[i % 2], draft, acc, nxt, stream=stream)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(reps):
+                bqd.spec_decode_verify(sets[i % 2], draft, acc, nxt, stream=stream)
+        for _ in range(3):
+            graph.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        e1.synchronize()
     us = e0.elapsed_time(e1) / reps * 1e3
     nbytes = B * (D + 1) * V * 2 + B * D * 4 + 2 * B * 4
-    del sets
+    del graph, sets
     return us, nbytes / (us * 1e-6) / 1e9
 
 

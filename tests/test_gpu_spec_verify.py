@@ -111,3 +111,27 @@ def test_argument_errors():
     a, n = bqd.spec_decode_verify(torch.zeros((0, 3, 10), dtype=torch.float16, device="cuda"),
                                   torch.zeros((0, 2), dtype=torch.int32, device="cuda"))
     assert a.numel() == 0 and n.numel() == 0
+
+
+@pytest.mark.parametrize("dtype", [np.float16, np.float32])
+def test_rows_split_over_the_cluster(dtype):
+    """Few rows: each row's vocabulary is split into parts reduced by different
+    CTAs (here 2 rows x 4 parts of ~5000, boundaries off 16-byte alignment).
+    Ties across parts go to the smaller token; NaN-only parts are ignored."""
+    B, D, V = 4, 1, 20003
+    logits, draft = make_case(21, B, D, V, dtype, plant=False)
+    logits[0, 0, [100, 12000, 20002]] = 30.0        # tie across parts 0, 2, 3: token 100
+    logits[1, 0, :5000] = np.nan                   # part 0 all NaN; maximum in part 3
+    logits[1, 0, 19000] = 30.0
+    draft[1, 0] = 19000
+    logits[2, :, :] = np.nan                       # every part NaN: -1
+    logits[3, 1, 10001] = 30.0                     # maximum at a part's first value
+    acc = run(logits, draft)
+    assert acc[1] == 1
+
+
+def test_small_batch_full_vocabulary():
+    """One sequence, 4 draft tokens, a 151,936-token vocabulary: the five rows
+    are split over the cluster's 15 CTAs."""
+    logits, draft = make_case(5, 1, 4, 151936, np.float16)
+    run(logits, draft)
