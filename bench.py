@@ -431,7 +431,7 @@ def kernel_traffic_from_profiles():
 
 def run_case(spec: str, sets: int, reps: int = 64):
     """--case fmt,M,N,K,gs[,sym]: one configuration over rotating weight sets
-    (the driver used for single-kernel ncu captures)."""
+    (the command line used for single-kernel ncu captures)."""
     import torch
     import bit_quantized_decode_unpack_gb300 as bqd
     from bit_quantized_decode_unpack_gb300 import _build, synth
