@@ -506,14 +506,14 @@ def reference_arm(args):
     """The float64 oracle as the reference arm, on host cores: every step is
     a bounded sample of the same workload (the first R weight rows of a
     stride-j subset of the 280 calls), sized so that the whole run ends
-    within about two minutes."""
+    within about two minutes (--ref-budget)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     import oracle
     oracle.build()
     calls = sweep_calls()
-    budget = 120.0 / max(1, args.steps + args.warmup)  # seconds per step
+    budget = args.ref_budget / max(1, args.steps + args.warmup)  # seconds per step
     _, per_row = calibrate_rows(calls, 1.0)
     stride = 1
     while per_row / stride > budget and stride < len(calls):
@@ -555,6 +555,8 @@ def main():
     ap.add_argument("--no-qmm", action="store_true", help="skip the prefill matrix-product timings")
     ap.add_argument("--no-spec", action="store_true", help="skip the speculative-decoding verification timing")
     ap.add_argument("--cpu-rows", type=int, default=0, help="0: sized for ~12 s of oracle work")
+    ap.add_argument("--ref-budget", type=float, default=120.0,
+                    help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--case", type=str, default=None, help="fmt,M,N,K,gs[,sym]: time one configuration")
     ap.add_argument("--spec-case", type=str, default=None,
                     help="B,D,V: time the speculative-decoding verification on fp16 logits")
