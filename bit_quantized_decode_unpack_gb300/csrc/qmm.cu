@@ -187,13 +187,13 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c)
 // NH = 2: the CTA owns two 256-column blocks of x (two N=256 accumulators,
 // all 512 TMEM columns), so each decoded weight tile serves 512 columns; its
 // K step is then 64 codes (half a 128-group), which keeps two stages of
-// [A 16 KB | X 64 KB] in shared memory.  1/2-bit only (t5 groups are not
-// byte-aligned at 32-code boundaries).
+// [A 16 KB | X 64 KB] in shared memory.  1/2-bit, and t5 at gs=64 (a 128-code
+// t5 group cannot be split into byte-aligned 32-code quarters).
 template <int FMT, int GS, int NH>
 __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParams &p)
 {
     constexpr bool T5F = FMT == BQD_FMT_T5;
-    static_assert(NH == 1 || (!T5F && NH == 2), "two column blocks per CTA: 1/2-bit only");
+    static_assert(NH == 1 || (NH == 2 && (!T5F || GS == 64)), "two column blocks: 1/2-bit or t5 at gs=64");
     constexpr int KS = NH == 2 ? 64 : GS;  // codes per K step
     constexpr int SPG = GS / KS;           // K steps per group (1 or 2)
     constexpr int B = GS == 64 ? 13 : 26;  // t5 bytes per group
@@ -522,7 +522,7 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
             }
             return true;
         };
-        if constexpr (NH == 2) {
+        if constexpr (NH == 2 && !T5F) {
             // 64-code steps are short: two steps of bytes, scale and bias are in
             // flight per thread, in two register slots used alternately (two
             // steps per iteration, so the slot of each load is a constant).
@@ -655,11 +655,11 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
     if (warp == kMmaWarpQ) tmem_dealloc(tmem, (uint32_t)C);
 }
 
-template <int GS>
+template <int GS, int NH>
 __global__ void __launch_bounds__(kThreadsQ, 1)
 qmm_t5_kernel(const __grid_constant__ CUtensorMap xmap, const QmmParams p)
 {
-    qmm_body<BQD_FMT_T5, GS, 1>(xmap, p);
+    qmm_body<BQD_FMT_T5, GS, NH>(xmap, p);
 }
 
 template <int FMT, int GS, int NH>
@@ -691,7 +691,7 @@ int launch_gs(const QmmParams &p, const CUtensorMap &map, int tiles, size_t smem
 {
     void (*kern)(const CUtensorMap, const QmmParams);
     if constexpr (FMT == BQD_FMT_T5)
-        kern = qmm_t5_kernel<GS>;
+        kern = qmm_t5_kernel<GS, NH>;
     else
         kern = qmm_affine_kernel<FMT, GS, NH>;
     static int configured_dev[64] = {0};
@@ -751,11 +751,11 @@ int launch_qmm(const QmvArgs &a, cudaStream_t s)
     p.row_bytes = a.row_bytes;
     p.zero = 0;
     p.bx = a.M <= 32 ? 32 : (a.M <= 64 ? 64 : (a.M <= 128 ? 128 : 256));
-    // 1/2-bit with more than 256 x rows on a wide layer: two 256-column blocks
-    // per CTA (the decoded weight tile serves 512 columns), K steps of 64
-    // codes.  Narrow layers keep one block: their few 128-row tiles would
+    // 1/2-bit (and t5 at gs=64) with more than 256 x rows on a wide layer: two
+    // 256-column blocks per CTA (the decoded weight tile serves 512 columns),
+    // K steps of 64 codes.  Narrow layers keep one block: their few 128-row tiles would
     // leave SMs idle (measured: down projection, M=512, 813 -> 470 TFLOP/s)
-    const bool pair = a.fmt != BQD_FMT_T5 && a.M > 256 && a.N >= 8192;
+    const bool pair = (a.fmt != BQD_FMT_T5 || a.gs == 64) && a.M > 256 && a.N >= 8192;
     const int NH = pair ? 2 : 1;
     const int KS = pair ? 64 : a.gs;
     const int cols = NH * p.bx;
@@ -788,9 +788,11 @@ int launch_qmm(const QmvArgs &a, cudaStream_t s)
     if (getenv("BQD_DEBUG_PLAN"))
         fprintf(stderr, "bqd qmm plan: fmt=%d M=%d N=%d K=%d gs=%d -> bx=%d x%d tiles=%d S=%d gpr=%d stages=%d smem=%zu\n",
                 a.fmt, p.M, p.N, p.K, a.gs, p.bx, NH, tiles, S, p.gpr, p.stages, smem);
-    if (a.fmt == BQD_FMT_T5)
+    if (a.fmt == BQD_FMT_T5) {
+        if (pair) return launch_gs<BQD_FMT_T5, 64, 2>(p, map, tiles, smem, s);
         return a.gs == 64 ? launch_gs<BQD_FMT_T5, 64, 1>(p, map, tiles, smem, s)
                           : launch_gs<BQD_FMT_T5, 128, 1>(p, map, tiles, smem, s);
+    }
     if (a.fmt == BQD_FMT_AFFINE2) {
         if (pair)
             return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE2, 64, 2>(p, map, tiles, smem, s)

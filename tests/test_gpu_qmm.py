@@ -142,6 +142,20 @@ def test_affine_two_column_blocks_per_cta(fmt, gs, sym):
         run(p, m_rows=m_rows, n_rows=n_rows)
 
 
+@pytest.mark.parametrize("bias", [False, True])
+def test_t5_gs64_two_column_blocks_per_cta(bias):
+    """t5 at gs=64 takes the two-block mode too (its 64-code groups split into
+    byte-aligned 32-code halves); sampled outputs as above."""
+    rng = np.random.default_rng(64 + bias)
+    for M, N, K in [(300, 8200, 1024), (513, 8192, 1024)]:
+        p = synth.problem(T5, M, N, K, 64, sym=True)
+        if bias:
+            p["biases"] = synth.biases(rng, F2, p["scales"])
+        m_rows = np.unique(np.concatenate([[0, 255, 256, M - 1], rng.integers(0, M, 12)]))
+        n_rows = np.unique(np.concatenate([[0, 127, 4096, N - 1], rng.integers(0, N, 12)]))
+        run(p, m_rows=m_rows, n_rows=n_rows)
+
+
 @pytest.mark.parametrize("fmt", [F1, F2, T5])
 @pytest.mark.parametrize("gs", [64, 128])
 def test_forced_product_at_decode_sizes(fmt, gs):
