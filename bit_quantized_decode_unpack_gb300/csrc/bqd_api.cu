@@ -26,9 +26,9 @@ int sm_count()
 // Testing override of the dispatcher: BQD_FORCE_KERNEL=generic|mma|tma|qmm
 // (read on every call so that a test can compare the kernels in one process).
 // "mma" forces the register-streaming tensor-core kernels (the prefill
-// product for M > 16), "tma" the TMA-ring decode kernels at any M, "qmm" the
-// tcgen05 prefill product at any M; a forced kernel's "unsupported" is
-// returned as is.
+// product where M is prefill-sized), "tma" the TMA-ring decode kernels at any
+// M, "qmm" the tcgen05 prefill product at any M; a forced kernel's
+// "unsupported" is returned as is.
 static int forced_kernel()
 {
     const char *v = getenv("BQD_FORCE_KERNEL");

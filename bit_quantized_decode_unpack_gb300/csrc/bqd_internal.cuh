@@ -44,7 +44,7 @@ int launch_qmv_tma(const QmvArgs &a, cudaStream_t s);
 int launch_qmv_t5r(const QmvArgs &a, cudaStream_t s);
 // Tensor-core decode path for t5 weights (K a multiple of 1024); same contract.
 int launch_qmv_t5(const QmvArgs &a, cudaStream_t s);
-// Prefill matrix product on tcgen05 tensor cores (meant for M > 16), every
+// Prefill matrix product on tcgen05 tensor cores (for prefill-sized M), every
 // format (16-byte aligned weight base; t5 rows a multiple of 16 bytes).
 int launch_qmm(const QmvArgs &a, cudaStream_t s);
 
