@@ -38,12 +38,13 @@ UNIT = "GB/s"
 WORKLOAD = ("full decode sweep, 27B-class layer: 7 projections (q 6144x5120, k/v 1024x5120, "
             "o 5120x6144, gate/up 17408x5120, down 5120x17408) x M 1..5 x {1-bit, 2-bit, "
             "2-bit sym, t5} x group_size {64,128} = 280 QMV calls per step; 64 rotating "
-            "weight sets per projection/format/group size")
+            "weight sets per projection/group size, each call of a step on its own set")
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 F1, F2, T5 = 1, 2, 3
 VARIANTS = [("affine1", F1, False), ("affine2", F2, False), ("affine2_sym", F2, True), ("t5", T5, True)]
+VARIANT_INDEX = {v[0]: i for i, v in enumerate(VARIANTS)}
 GROUP_SIZES = (64, 128)
 MS = (1, 2, 3, 4, 5)
 
@@ -210,6 +211,14 @@ class Sweep:
         self.d2h = sum(c["M"] * c["N"] * 2 for c in self.calls)
         torch.cuda.synchronize()
 
+    def set_index(self, q, c):
+        """Weight set of call c in graph phase q.  Each variant takes its own
+        window of the rotation (offset 16 sets per variant), so within a
+        step no two calls share a packed matrix or a scale or bias tensor
+        (every format's weights of one set share that set's scales): every
+        call streams bytes that no other call of the step has read."""
+        return (5 * q + c["M"] - 1 + 16 * VARIANT_INDEX[c["variant"]]) % self.sets
+
     def _call(self, i, c, set_idx, stream):
         torch = self.torch
         e = self.weights[(c["proj"], c["gs"])][set_idx]
@@ -223,7 +232,7 @@ class Sweep:
         self.bqd.qmv(x, w, e["scales"], b, c["fmt"], c["gs"], out=y, stream=stream)
 
     def capture(self, n_graphs: int):
-        """One graph per step phase; phase q uses set (5q + M - 1) mod sets."""
+        """One graph per step phase q (weight sets from set_index)."""
         torch = self.torch
         self.stream = torch.cuda.Stream()
         self.graphs = []
@@ -231,12 +240,12 @@ class Sweep:
             for q in range(n_graphs):
                 # warm (outside capture) once, then capture
                 for i, c in enumerate(self.calls):
-                    self._call(i, c, (5 * q + c["M"] - 1) % self.sets, self.stream)
+                    self._call(i, c, self.set_index(q, c), self.stream)
                 self.stream.synchronize()
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=self.stream):
                     for i, c in enumerate(self.calls):
-                        self._call(i, c, (5 * q + c["M"] - 1) % self.sets, self.stream)
+                        self._call(i, c, self.set_index(q, c), self.stream)
                 self.graphs.append(g)
         torch.cuda.synchronize()
 
@@ -280,36 +289,144 @@ def time_steps(sweep, steps, warmup, e2e=False, barrier=None):
     return t0.elapsed_time(t1)  # ms
 
 
-def per_call_table(sweep, reps: int = 3):
-    """µs per call and effective GB/s for each (projection, variant, gs, M),
-    each timed as a graph of `sets` back-to-back calls over the rotating sets."""
+def _graph_calls(sweep, calls_fn, n, st):
+    """Capture n calls (calls_fn(j) enqueues call j) into CUDA graphs of at
+    most 1024 calls each, after one warm pass outside capture."""
     torch = sweep.torch
-    rows = []
-    st = sweep.stream
-    for i, c in enumerate(sweep.calls):
-        with torch.cuda.stream(st):
-            for s in range(sweep.sets):
-                sweep._call(i, c, s, st)
-            st.synchronize()
+    graphs = []
+    with torch.cuda.stream(st):
+        for j in range(n):
+            calls_fn(j)
+        st.synchronize()
+        for j0 in range(0, n, 1024):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=st):
-                for s in range(sweep.sets):
-                    sweep._call(i, c, s, st)
-        best = None
-        with torch.cuda.stream(st):
-            for _ in range(reps):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(st)
+                for j in range(j0, min(n, j0 + 1024)):
+                    calls_fn(j)
+            graphs.append(g)
+    return graphs
+
+
+def time_call(sweep, c, W, x, y, reps: int = 3):
+    """µs per call of configuration c: CUDA graphs of back-to-back calls, one
+    per weight set of W (enough sets that together they exceed the L2), best
+    of `reps` replays of the whole rotation."""
+    torch = sweep.torch
+    st = sweep.stream
+
+    def one(j):
+        e = W[j]
+        w = {F1: e.get("w1"), F2: e.get("w2"), T5: e.get("w5")}[c["fmt"]]
+        b = None if c["sym"] else (e["b1"] if c["fmt"] == F1 else e["b2"])
+        sweep.bqd.qmv(x, w, e["scales"], b, c["fmt"], c["gs"], out=y, stream=st)
+
+    graphs = _graph_calls(sweep, one, len(W), st)
+    best = None
+    with torch.cuda.stream(st):
+        for g in graphs:  # warm replay
+            g.replay()
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for g in graphs:
                 g.replay()
-                e1.record(st)
-                e1.synchronize()
-                t = e0.elapsed_time(e1) * 1e3 / sweep.sets
-                best = t if best is None else min(best, t)
-        nb = call_bytes(c["fmt"], c["sym"], c["M"], c["N"], c["K"], c["gs"])
-        rows.append(dict(proj=c["proj"], variant=c["variant"], gs=c["gs"], M=c["M"], us=round(best, 3),
-                         gbs=round(nb / (best * 1e-6) / 1e9, 1)))
-        del g
+            e1.record(st)
+            e1.synchronize()
+            t = e0.elapsed_time(e1) * 1e3 / len(W)
+            best = t if best is None else min(best, t)
+    del graphs
+    return best
+
+
+def per_call_table(sweep, calls, weights, reps: int = 3):
+    """µs per call and effective GB/s for each configuration in `calls`
+    (dicts as sweep_calls() makes), each timed over the rotating weight sets
+    weights[(proj, gs)]."""
+    torch = sweep.torch
+    rows = []
+    gen = torch.Generator(device=sweep.dev)
+    gen.manual_seed(99)
+    from bit_quantized_decode_unpack_gb300 import synth
+    for c in calls:
+        M, N, K = c["M"], c["N"], c["K"]
+        x = synth.torch_activations(gen, M, K, sweep.dev)
+        y = torch.empty((M, N), dtype=torch.float16, device=sweep.dev)
+        us = time_call(sweep, c, weights[(c["proj"], c["gs"])], x, y, reps)
+        nb = call_bytes(c["fmt"], c["sym"], M, N, K, c["gs"])
+        rows.append(dict(proj=c["proj"], variant=c["variant"], gs=c["gs"], M=M, N=N, K=K, bytes=nb,
+                         us=round(us, 3), gbs=round(nb / (us * 1e-6) / 1e9, 1)))
+        del x, y
     return rows
+
+
+def aggregate(rows, key):
+    """Sum of bytes over sum of time, per key(row)."""
+    acc = {}
+    for r in rows:
+        k = key(r)
+        b, t = acc.get(k, (0, 0.0))
+        acc[k] = (b + r["bytes"], t + r["us"])
+    return {k: {"gbs": round(b / (t * 1e-6) / 1e9, 1), "us": round(t, 2)} for k, (b, t) in acc.items()}
+
+
+def make_weight_sets(sweep, name, N, K, gs, fmts, sets, seed):
+    """`sets` weight sets of (N, K, gs) for the formats in `fmts` (packed on
+    the device), with their scales and 1/2-bit biases."""
+    torch = sweep.torch
+    from bit_quantized_decode_unpack_gb300 import synth
+    gen = torch.Generator(device=sweep.dev)
+    gen.manual_seed(seed)
+    lst = []
+    for _ in range(sets):
+        s_ = synth.torch_scales(gen, N, K // gs, sweep.dev)
+        e = {"scales": s_}
+        if F1 in fmts:
+            e["b1"] = synth.torch_biases(gen, F1, s_, sweep.dev)
+        if F2 in fmts:
+            e["b2"] = synth.torch_biases(gen, F2, s_, sweep.dev)
+        for fmt, key in ((F1, "w1"), (F2, "w2"), (T5, "w5")):
+            if fmt in fmts:
+                e[key] = sweep.bqd.pack(synth.torch_codes(gen, fmt, N, K, sweep.dev), fmt, gs)
+        lst.append(e)
+    return lst
+
+
+def config_tables(sweep, sweep_rows):
+    """The three single-format configurations, each as per-call rows and one
+    aggregate (bytes of all its calls / time of all its calls):
+      config 1: 1-bit, M=1, N=256, K=512, gs=64 (8192 rotating sets, 196 MB);
+      config 2: 2-bit asym + sym, M 1..5, gs 64/128, (N,K) in {(5120,5120),
+                (1024,5120), (17408,5120), (5120,17408)};
+      config 3: t5, M 1..5, gs 64/128, (N,K) in {(17408,5120), (5120,17408)}.
+    Shapes that the sweep already timed reuse its rows; 5120x5120 and the
+    1-bit 256x512 case are timed here."""
+    torch = sweep.torch
+    out = {}
+    # config 1
+    W1 = make_weight_sets(sweep, "c1", 256, 512, 64, (F1,), 8192, seed=11)
+    c1 = [dict(M=1, proj="c1_256x512", N=256, K=512, variant="affine1", fmt=F1, sym=False, gs=64)]
+    r1 = per_call_table(sweep, c1, {("c1_256x512", 64): W1})
+    del W1
+    out["config1_affine1_256x512_m1_gs64"] = {"rows": r1, **aggregate(r1, lambda r: "all")["all"]}
+    # config 2: the sweep's k/gate/down rows plus 5120x5120
+    extra = {}
+    for gs in GROUP_SIZES:
+        extra[("sq_5120", gs)] = make_weight_sets(sweep, "sq", 5120, 5120, gs, (F2,), 64, seed=20 + gs)
+    c2_new = [dict(M=M, proj="sq_5120", N=5120, K=5120, variant=v, fmt=F2, sym=sym, gs=gs)
+              for M in MS for v, sym in (("affine2", False), ("affine2_sym", True)) for gs in GROUP_SIZES]
+    r2 = per_call_table(sweep, c2_new, extra)
+    del extra
+    r2 += [r for r in sweep_rows if r["variant"] in ("affine2", "affine2_sym")
+           and r["proj"] in ("k_proj", "gate_proj", "down_proj")]
+    out["config2_affine2"] = {"rows": len(r2), **aggregate(r2, lambda r: "all")["all"],
+                              "by_shape": aggregate(r2, lambda r: f"{r['N']}x{r['K']}"),
+                              "by_m": aggregate(r2, lambda r: f"M{r['M']}")}
+    r3 = [r for r in sweep_rows if r["variant"] == "t5" and r["proj"] in ("gate_proj", "down_proj")]
+    out["config3_t5"] = {"rows": len(r3), **aggregate(r3, lambda r: "all")["all"],
+                         "by_shape": aggregate(r3, lambda r: f"{r['N']}x{r['K']}"),
+                         "by_m": aggregate(r3, lambda r: f"M{r['M']}")}
+    torch.cuda.synchronize()
+    return out
 
 
 QMM_CASES = [(M, N, K) for M in (32, 512, 2048) for (N, K) in [(17408, 5120), (5120, 17408)]]
@@ -317,20 +434,17 @@ QMM_CASES = [(M, N, K) for M in (32, 512, 2048) for (N, K) in [(17408, 5120), (5
 
 def time_qmm(dev, fmt: int, reps: int = 10):
     """The tcgen05 prefill matrix product of one format, gs=128: TFLOP/s per
-    case (2*M*N*K flops).  The product is forced (BQD_FORCE_KERNEL=qmm) so that
-    each case times that kernel, whatever the dispatcher would pick at that M.
+    case (2*M*N*K flops).  The product is forced (bqd_set_option) so that each
+    case times that kernel, whatever the dispatcher would pick at that M.
     Each case rotates through enough weight sets (codes, scales, biases for
     1/2-bit) to exceed the 129 MB L2."""
-    import os
-    old = os.environ.get("BQD_FORCE_KERNEL")
-    os.environ["BQD_FORCE_KERNEL"] = "qmm"
+    import bit_quantized_decode_unpack_gb300 as bqd
+    old = bqd.get_option(bqd.OPT_KERNEL)
+    bqd.force_kernel("qmm")
     try:
         return _time_qmm(dev, fmt, reps)
     finally:
-        if old is None:
-            os.environ.pop("BQD_FORCE_KERNEL", None)
-        else:
-            os.environ["BQD_FORCE_KERNEL"] = old
+        bqd.set_option(bqd.OPT_KERNEL, old)
 
 
 def _time_qmm(dev, fmt: int, reps: int):
@@ -469,14 +583,26 @@ def run_case(spec: str, sets: int, reps: int = 64):
 
 # ---- CPU baseline / reference arm (the oracle on host cores) ----------------------
 
-def oracle_sample(rows_per_call: int, calls, seed=0):
+def host_cores() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(rows_per_call: int, calls, seed=0, threads: int = 1):
     """Time the float64 oracle on the first `rows_per_call` weight rows of each
-    call (same distributions).  Returns (bytes, seconds)."""
+    call (same distributions).  With threads > 1 the rows of each call are
+    split into contiguous ranges, one per thread (the C oracle runs without
+    the interpreter lock).  Returns (bytes, seconds)."""
     import numpy as np
     import oracle
+    from concurrent.futures import ThreadPoolExecutor
     from bit_quantized_decode_unpack_gb300 import synth
     tot_b, tot_t = 0, 0.0
     cache = {}
+    pool = ThreadPoolExecutor(threads) if threads > 1 else None
     for c in calls:
         key = (c["proj"], c["variant"], c["gs"])
         if key not in cache:
@@ -489,9 +615,18 @@ def oracle_sample(rows_per_call: int, calls, seed=0):
         packed, s, b = cache[key]
         x = synth.activations(np.random.default_rng(c["M"]), c["M"], c["K"])
         t = time.perf_counter()
-        oracle.c_qmv_rows(x, packed, s, b, c["fmt"], c["gs"])
+        if pool is None:
+            oracle.c_qmv_rows(x, packed, s, b, c["fmt"], c["gs"])
+        else:
+            edges = np.linspace(0, rows_per_call, threads + 1).astype(np.int64)
+            futs = [pool.submit(oracle.c_qmv_rows, x, packed, s, b, c["fmt"], c["gs"], np.arange(lo, hi))
+                    for lo, hi in zip(edges[:-1], edges[1:]) if hi > lo]
+            for f in futs:
+                f.result()
         tot_t += time.perf_counter() - t
         tot_b += call_bytes(c["fmt"], c["sym"], c["M"], rows_per_call, c["K"], c["gs"])
+    if pool is not None:
+        pool.shutdown()
     return tot_b, tot_t
 
 
@@ -503,38 +638,41 @@ def calibrate_rows(calls, seconds: float, cap: int = 256):
 
 
 def reference_arm(args):
-    """The float64 oracle as the reference arm, on host cores: every step is
-    a bounded sample of the same workload (the first R weight rows of a
-    stride-j subset of the 280 calls), sized so that the whole run ends
-    within about two minutes (--ref-budget)."""
+    """The float64 oracle as the reference arm, on all host cores: every
+    step is a bounded sample of the same workload (the first R weight rows of
+    a stride-j subset of the 280 calls, the rows of each call split over the
+    cores), sized so that the whole run ends within about two minutes
+    (--ref-budget)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     import oracle
     oracle.build()
     calls = sweep_calls()
+    cores = host_cores()
     budget = args.ref_budget / max(1, args.steps + args.warmup)  # seconds per step
     _, per_row = calibrate_rows(calls, 1.0)
+    per_row /= cores  # rows are split over the cores
     stride = 1
-    while per_row / stride > budget and stride < len(calls):
+    while per_row / stride > budget / 8 and stride < len(calls):
         stride *= 2
     sub = calls[::stride]
-    rows = max(1, min(64, int(budget / max(per_row / stride, 1e-9))))
+    rows = max(cores, min(64 * cores, int(budget / max(per_row * len(sub), 1e-9))))
     for _ in range(args.warmup):
-        oracle_sample(rows, sub)
+        oracle_sample(rows, sub, threads=cores)
     b = t = 0.0
     for _ in range(args.steps):
-        bb, tt = oracle_sample(rows, sub)
+        bb, tt = oracle_sample(rows, sub, threads=cores)
         b += bb
         t += tt
     value = b / t / 1e9
     sample = (f"first {rows} weight rows of " + ("each" if stride == 1 else f"every {stride}th") +
-              " of the 280 calls, per step")
+              f" of the 280 calls, per step, rows split over {cores} threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -550,7 +688,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sets", type=int, default=64)
     ap.add_argument("--quick", action="store_true", help="two projections only (development)")
-    ap.add_argument("--table", type=str, default=None, help="write the per-call table (CSV) here")
+    ap.add_argument("--table", type=str, default=None, help="also write the per-call table (CSV) here")
+    ap.add_argument("--no-table", action="store_true", help="skip the per-call table and the config figures")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-qmm", action="store_true", help="skip the prefill matrix-product timings")
     ap.add_argument("--no-spec", action="store_true", help="skip the speculative-decoding verification timing")
@@ -607,13 +746,16 @@ def main():
     value = whole_job_gbs(sweep.bytes_per_step, args.steps, world, ms)
     value_e2e = whole_job_gbs(sweep.bytes_per_step, args.steps, world, ms_e2e)
 
-    table = None
-    if rank == 0 and args.table:
-        table = per_call_table(sweep)
-        with open(args.table, "w") as f:
-            f.write("proj,variant,gs,M,us_per_call,gbs\n")
-            for r in table:
-                f.write(f"{r['proj']},{r['variant']},{r['gs']},{r['M']},{r['us']},{r['gbs']}\n")
+    table = configs = None
+    if rank == 0 and not args.no_table:
+        table = per_call_table(sweep, sweep.calls, sweep.weights)
+        if args.table:
+            with open(args.table, "w") as f:
+                f.write("proj,variant,gs,M,us_per_call,gbs\n")
+                for r in table:
+                    f.write(f"{r['proj']},{r['variant']},{r['gs']},{r['M']},{r['us']},{r['gbs']}\n")
+        if not args.quick:
+            configs = config_tables(sweep, table)
 
     if rank == 0:
         peaks, src = load_peaks()
@@ -641,6 +783,17 @@ def main():
             "gpu_launches": len(sweep.calls) * args.steps,
             "clocks": clocks,
         }
+        if table is not None:
+            line["per_call"] = {
+                "columns": ["proj", "variant", "gs", "M", "us", "gbs"],
+                "how": "graph of back-to-back calls of one configuration over its 64 rotating weight sets; "
+                       "best of 3 replays",
+                "rows": [[r["proj"], r["variant"], r["gs"], r["M"], r["us"], r["gbs"]] for r in table]}
+            line["per_format_m"] = aggregate(table, lambda r: f"{r['variant']}/M{r['M']}")
+            line["per_format"] = aggregate(table, lambda r: r["variant"])
+            line["per_projection"] = aggregate(table, lambda r: r["proj"])
+        if configs is not None:
+            line["configs"] = configs
         if not args.no_qmm:
             tf_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
             for key, fmt, label in (("qmm", T5, "t5"), ("qmm_affine2", F2, "2-bit affine"),
@@ -665,9 +818,16 @@ def main():
             oracle.build()
             rows = args.cpu_rows or calibrate_rows(sweep_calls(), 12.0)[0]
             b, t = oracle_sample(rows, sweep_calls())
-            line["cpu_baseline"] = {"value": b / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                    "sample": f"first {rows} weight rows of each of the 280 calls "
-                                              f"({t:.1f} s, one thread)"}
+            cores = host_cores()
+            rows_mt = rows * cores
+            b_mt, t_mt = oracle_sample(rows_mt, sweep_calls(), threads=cores)
+            line["cpu_baseline"] = {"value": b_mt / t_mt / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                    "sample": f"first {rows_mt} weight rows of each of the 280 calls, rows split "
+                                              f"over {cores} threads ({t_mt:.1f} s)",
+                                    "single_thread": {"value": b / t / 1e9, "unit": UNIT, "cores": 1,
+                                                      "sample": f"first {rows} weight rows of each of the 280 "
+                                                                f"calls ({t:.1f} s)"},
+                                    "host_cpu_count": os.cpu_count()}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()

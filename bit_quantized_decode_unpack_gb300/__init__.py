@@ -25,6 +25,8 @@ DTYPE_F16 = 1
 DTYPE_F32 = 2
 
 BQD_OK = 0
+OPT_KERNEL, OPT_T5_STAGES, OPT_WAIT_LIMIT_NS, OPT_DEBUG_PLAN = 1, 2, 3, 4
+KERNELS = {None: 0, "auto": 0, "generic": 1, "mma": 2, "tma": 3, "qmm": 4}
 ABI_VERSION = 1  # must match BQD_ABI_VERSION in include/bqd.h
 
 _PKG = Path(__file__).resolve().parent
@@ -75,6 +77,10 @@ def load() -> ctypes.CDLL:
         lib.bqd_spec_decode_verify.restype = i32
         lib.bqd_device_status.argtypes = [vp]
         lib.bqd_device_status.restype = i32
+        lib.bqd_set_option.argtypes = [i32, i64]
+        lib.bqd_set_option.restype = i32
+        lib.bqd_get_option.argtypes = [i32]
+        lib.bqd_get_option.restype = i64
         if lib.bqd_abi_version() != ABI_VERSION:
             raise RuntimeError(f"libbqd ABI {lib.bqd_abi_version()} != binding ABI {ABI_VERSION}")
         _lib = lib
@@ -101,6 +107,61 @@ def _fmt(fmt) -> int:
     return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
 
 
+def _need(t, name, *, dtype=None, shape=None, nbytes=None, device=None, min_numel=None):
+    """Check a tensor argument before its address is handed to the library:
+    a CUDA tensor, contiguous, of the expected dtype, shape or byte size, on
+    the expected device.  A wrong buffer would otherwise let a kernel read or
+    write past an allocation.  Raises ValueError."""
+    if t is None:
+        raise ValueError(f"{name}: a tensor is required")
+    if not getattr(t, "is_cuda", False):
+        raise ValueError(f"{name}: must be a CUDA tensor (got device {getattr(t, 'device', None)})")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous (row-major, no strides)")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if nbytes is not None and t.numel() * t.element_size() != nbytes:
+        raise ValueError(f"{name}: {t.numel() * t.element_size()} bytes, expected {nbytes}")
+    if min_numel is not None and t.numel() < min_numel:
+        raise ValueError(f"{name}: {t.numel()} elements, expected at least {min_numel}")
+    return t
+
+
+def _check_group(K: int, group_size: int):
+    if group_size not in (64, 128):
+        raise ValueError(f"group_size must be 64 or 128, got {group_size}")
+    if K % group_size != 0:
+        raise ValueError(f"K={K} is not a multiple of group_size={group_size}")
+
+
+def _check_qmv_args(x, w_packed, scales, biases, fmt, group_size, out):
+    import torch
+    f16 = torch.float16
+    if getattr(x, "dim", lambda: 0)() != 2:
+        raise ValueError("x must be a 2-D fp16 tensor [M, K]")
+    if getattr(scales, "dim", lambda: 0)() != 2:
+        raise ValueError("scales must be a 2-D fp16 tensor [N, G]")
+    M, K = x.shape
+    N, G = scales.shape
+    f = _fmt(fmt)
+    if f not in FORMATS.values():
+        raise ValueError(f"unknown format {fmt!r}")
+    _check_group(K, group_size)
+    dev = x.device
+    _need(x, "x", dtype=f16, device=dev)
+    _need(scales, "scales", dtype=f16, shape=(N, K // group_size), device=dev)
+    _need(w_packed, "w_packed", nbytes=packed_bytes(f, N, K, group_size), device=dev)
+    if biases is not None:
+        _need(biases, "biases", dtype=f16, shape=(N, G), device=dev)
+    if out is not None:
+        _need(out, "out", dtype=f16, shape=(M, N), device=dev)
+    return M, N, K
+
+
 # ---- host-only entry points ----------------------------------------------
 
 def abi_version() -> int:
@@ -125,8 +186,7 @@ def qmv(x, w_packed, scales, biases, fmt, group_size: int, out=None, stream=None
     """y = x @ dequant(W)^T, fp16 [M, N].  ``biases=None`` selects the sym
     path (no bias tensor read, default ratio of the format)."""
     import torch
-    M, K = x.shape
-    N = scales.shape[0]
+    M, N, K = _check_qmv_args(x, w_packed, scales, biases, fmt, group_size, out)
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=x.device)
     _check("bqd_qmv", load().bqd_qmv(_ptr(x), _ptr(w_packed), _ptr(scales), _ptr(biases), M, N, K,
@@ -137,8 +197,7 @@ def qmv(x, w_packed, scales, biases, fmt, group_size: int, out=None, stream=None
 def qmv_sym(x, w_packed, scales, ratio: float, fmt, group_size: int, out=None, stream=None):
     """Sym variant with an explicit ratio (bias = -ratio * scale, not read)."""
     import torch
-    M, K = x.shape
-    N = scales.shape[0]
+    M, N, K = _check_qmv_args(x, w_packed, scales, None, fmt, group_size, out)
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=x.device)
     _check("bqd_qmv_sym", load().bqd_qmv_sym(_ptr(x), _ptr(w_packed), _ptr(scales), float(ratio), M, N,
@@ -149,10 +208,15 @@ def qmv_sym(x, w_packed, scales, ratio: float, fmt, group_size: int, out=None, s
 def pack(codes, fmt, group_size: int, out=None, stream=None):
     """codes uint8 [N, K] (device) -> packed uint8 [N, row_bytes] (device)."""
     import torch
+    if getattr(codes, "dim", lambda: 0)() != 2:
+        raise ValueError("codes must be a 2-D uint8 tensor [N, K]")
     N, K = codes.shape
+    _check_group(K, group_size)
+    _need(codes, "codes", dtype=torch.uint8)
     rb = row_bytes(fmt, K, group_size)
     if out is None:
         out = torch.empty((N, rb), dtype=torch.uint8, device=codes.device)
+    _need(out, "out", nbytes=N * rb, device=codes.device)
     _check("bqd_pack", load().bqd_pack(_ptr(codes), N, K, _fmt(fmt), group_size, _ptr(out),
                                        _stream(stream)))
     return out
@@ -160,8 +224,11 @@ def pack(codes, fmt, group_size: int, out=None, stream=None):
 
 def unpack(w_packed, N: int, K: int, fmt, group_size: int, out=None, stream=None):
     import torch
+    _check_group(K, group_size)
+    _need(w_packed, "w_packed", nbytes=packed_bytes(fmt, N, K, group_size))
     if out is None:
         out = torch.empty((N, K), dtype=torch.uint8, device=w_packed.device)
+    _need(out, "out", dtype=torch.uint8, shape=(N, K), device=w_packed.device)
     _check("bqd_unpack", load().bqd_unpack(_ptr(w_packed), N, K, _fmt(fmt), group_size, _ptr(out),
                                            _stream(stream)))
     return out
@@ -170,10 +237,14 @@ def unpack(w_packed, N: int, K: int, fmt, group_size: int, out=None, stream=None
 def repack_2bit_to_t5(w2, N: int, K: int, group_size: int, out=None, status=None, stream=None):
     """-> (w_t5 uint8 [N, G*ceil(gs/5)], status int32[1] = count of codes equal to 3)."""
     import torch
+    _check_group(K, group_size)
+    _need(w2, "w2", nbytes=packed_bytes(FMT_AFFINE2, N, K, group_size))
     if out is None:
         out = torch.empty((N, row_bytes(FMT_T5, K, group_size)), dtype=torch.uint8, device=w2.device)
     if status is None:
         status = torch.empty((1,), dtype=torch.int32, device=w2.device)
+    _need(out, "out", nbytes=packed_bytes(FMT_T5, N, K, group_size), device=w2.device)
+    _need(status, "status", dtype=torch.int32, device=w2.device, min_numel=1)
     _check("bqd_repack_2bit_to_t5", load().bqd_repack_2bit_to_t5(
         _ptr(w2), N, K, group_size, _ptr(out), _ptr(status), _stream(stream)))
     return out, status
@@ -182,8 +253,11 @@ def repack_2bit_to_t5(w2, N: int, K: int, group_size: int, out=None, status=None
 def validate_t5(w_t5, N: int, K: int, group_size: int, status=None, stream=None):
     """-> int32[1] device tensor: number of invalid t5 bytes."""
     import torch
+    _check_group(K, group_size)
+    _need(w_t5, "w_t5", nbytes=packed_bytes(FMT_T5, N, K, group_size))
     if status is None:
         status = torch.empty((1,), dtype=torch.int32, device=w_t5.device)
+    _need(status, "status", dtype=torch.int32, device=w_t5.device, min_numel=1)
     _check("bqd_validate_t5", load().bqd_validate_t5(_ptr(w_t5), N, K, group_size, _ptr(status),
                                                      _stream(stream)))
     return status
@@ -192,9 +266,14 @@ def validate_t5(w_t5, N: int, K: int, group_size: int, status=None, stream=None)
 def detect_sym(scales, biases, ratio: float, out=None, stream=None):
     """-> int32[1] device tensor: number of biases != fp16(-ratio * scale)."""
     import torch
+    if getattr(scales, "dim", lambda: 0)() != 2:
+        raise ValueError("scales must be a 2-D fp16 tensor [N, G]")
     N, G = scales.shape
+    _need(scales, "scales", dtype=torch.float16)
+    _need(biases, "biases", dtype=torch.float16, shape=(N, G), device=scales.device)
     if out is None:
         out = torch.empty((1,), dtype=torch.int32, device=scales.device)
+    _need(out, "out", dtype=torch.int32, device=scales.device, min_numel=1)
     _check("bqd_detect_sym", load().bqd_detect_sym(_ptr(scales), _ptr(biases), N, G, float(ratio),
                                                    _ptr(out), _stream(stream)))
     return out
@@ -207,7 +286,10 @@ def spec_decode_verify(logits, draft, accepted=None, next_token=None, argmax_out
     (accepted int32 [B], next_token int32 [B]); pass ``argmax_out`` (int32
     [B, D+1]) to also receive every row's argmax."""
     import torch
+    if getattr(logits, "dim", lambda: 0)() != 3:
+        raise ValueError("logits must be a 3-D tensor [B, D+1, V]")
     B, D1, V = logits.shape
+    _need(logits, "logits")
     if logits.dtype == torch.float16:
         dt = DTYPE_F16
     elif logits.dtype == torch.float32:
@@ -216,14 +298,39 @@ def spec_decode_verify(logits, draft, accepted=None, next_token=None, argmax_out
         raise TypeError(f"logits must be float16 or float32, got {logits.dtype}")
     if draft.dtype != torch.int32 or tuple(draft.shape) != (B, D1 - 1):
         raise ValueError(f"draft must be int32 [{B}, {D1 - 1}], got {draft.dtype} {tuple(draft.shape)}")
+    dev = logits.device
+    if D1 > 1:
+        _need(draft, "draft", dtype=torch.int32, device=dev)
+    if accepted is not None:
+        _need(accepted, "accepted", dtype=torch.int32, shape=(B,), device=dev)
+    if next_token is not None:
+        _need(next_token, "next_token", dtype=torch.int32, shape=(B,), device=dev)
+    if argmax_out is not None:
+        _need(argmax_out, "argmax_out", dtype=torch.int32, shape=(B, D1), device=dev)
     if accepted is None:
-        accepted = torch.empty((B,), dtype=torch.int32, device=logits.device)
+        accepted = torch.empty((B,), dtype=torch.int32, device=dev)
     if next_token is None:
-        next_token = torch.empty((B,), dtype=torch.int32, device=logits.device)
+        next_token = torch.empty((B,), dtype=torch.int32, device=dev)
     _check("bqd_spec_decode_verify", load().bqd_spec_decode_verify(
         _ptr(logits), dt, _ptr(draft) if D1 > 1 else None, B, D1 - 1, V, _ptr(accepted), _ptr(next_token),
         _ptr(argmax_out), _stream(stream)))
     return accepted, next_token
+
+
+def set_option(option: int, value: int) -> None:
+    """Process-wide option (bqd_set_option): OPT_KERNEL (see KERNELS),
+    OPT_T5_STAGES, OPT_WAIT_LIMIT_NS, OPT_DEBUG_PLAN."""
+    _check("bqd_set_option", load().bqd_set_option(int(option), int(value)))
+
+
+def get_option(option: int) -> int:
+    return int(load().bqd_get_option(int(option)))
+
+
+def force_kernel(name) -> None:
+    """Force one kernel family for every QMV call (None or "auto": the
+    dispatcher picks).  For tests and measurements."""
+    set_option(OPT_KERNEL, KERNELS[name])
 
 
 def device_status(stream=None) -> int:

@@ -4,6 +4,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "bqd_internal.cuh"
 
 namespace bqd {
@@ -23,21 +25,42 @@ int sm_count()
     return cached[dev];
 }
 
-// Testing override of the dispatcher: BQD_FORCE_KERNEL=generic|mma|tma|qmm
-// (read on every call so that a test can compare the kernels in one process).
-// "mma" forces the register-streaming tensor-core kernels (the prefill
-// product where M is prefill-sized), "tma" the TMA-ring decode kernels at any
-// M, "qmm" the tcgen05 prefill product at any M; a forced kernel's
-// "unsupported" is returned as is.
-static int forced_kernel()
+// Process-wide options (bqd_set_option).  The environment supplies their
+// first values -- BQD_FORCE_KERNEL=generic|mma|tma|qmm, BQD_T5_STAGES=1|2,
+// BQD_DEBUG_PLAN -- read once, on first use; afterwards only
+// bqd_set_option changes them, so no call pays for reading the environment.
+namespace {
+struct Options {
+    std::atomic<int> kernel{BQD_KERNEL_AUTO};
+    std::atomic<int> t5_stages{0};
+    std::atomic<int> debug_plan{0};
+    std::atomic<int64_t> wait_ns{kDefaultWaitNs};
+    Options()
+    {
+        if (const char *v = getenv("BQD_FORCE_KERNEL")) {
+            if (strcmp(v, "generic") == 0) kernel = BQD_KERNEL_GENERIC;
+            else if (strcmp(v, "mma") == 0) kernel = BQD_KERNEL_MMA;
+            else if (strcmp(v, "tma") == 0) kernel = BQD_KERNEL_TMA;
+            else if (strcmp(v, "qmm") == 0) kernel = BQD_KERNEL_QMM;
+        }
+        if (const char *v = getenv("BQD_T5_STAGES")) {
+            const int n = atoi(v);
+            t5_stages = (n == 1 || n == 2) ? n : 0;
+        }
+        debug_plan = getenv("BQD_DEBUG_PLAN") != nullptr;
+    }
+};
+Options &options()
 {
-    const char *v = getenv("BQD_FORCE_KERNEL");
-    if (v && strcmp(v, "generic") == 0) return 1;
-    if (v && strcmp(v, "mma") == 0) return 2;
-    if (v && strcmp(v, "tma") == 0) return 3;
-    if (v && strcmp(v, "qmm") == 0) return 4;
-    return 0;
+    static Options o;  // initialised once, thread-safely
+    return o;
 }
+}  // namespace
+
+int opt_kernel() { return options().kernel.load(std::memory_order_relaxed); }
+int opt_t5_stages() { return options().t5_stages.load(std::memory_order_relaxed); }
+bool opt_debug_plan() { return options().debug_plan.load(std::memory_order_relaxed) != 0; }
+uint64_t opt_wait_ns() { return (uint64_t)options().wait_ns.load(std::memory_order_relaxed); }
 
 }  // namespace bqd
 
@@ -103,7 +126,7 @@ static int qmv_common(const void *x, const void *w, const void *scales, const vo
     a.row_bytes = row_bytes_of(format, K, gs);
     a.out = static_cast<__half *>(out);
 
-    const int force = forced_kernel();
+    const int force = opt_kernel();
     if (force != 1) {
         // prefill: fused unpack + tcgen05 matrix product.  Below these sizes the
         // decode kernels (all passes of their x rows in one launch) are faster
@@ -244,4 +267,39 @@ extern "C" int bqd_device_status(bqd_stream_t stream)
     st = take_qmv_t5r_timeouts(&n5);
     if (st != BQD_OK) return st;
     return (n1 || n2 || n3 || n4 || n5) ? BQD_ERR_TIMEOUT : BQD_OK;
+}
+
+extern "C" int bqd_set_option(int option, int64_t value)
+{
+    Options &o = options();
+    switch (option) {
+    case BQD_OPT_KERNEL:
+        if (value < BQD_KERNEL_AUTO || value > BQD_KERNEL_QMM) return BQD_ERR_INVALID_ARG;
+        o.kernel = (int)value;
+        return BQD_OK;
+    case BQD_OPT_T5_STAGES:
+        if (value < 0 || value > 2) return BQD_ERR_INVALID_ARG;
+        o.t5_stages = (int)value;
+        return BQD_OK;
+    case BQD_OPT_DEBUG_PLAN:
+        o.debug_plan = value != 0;
+        return BQD_OK;
+    case BQD_OPT_WAIT_LIMIT_NS:
+        if (value < 0) return BQD_ERR_INVALID_ARG;
+        o.wait_ns = value == 0 ? kDefaultWaitNs : value;
+        return BQD_OK;
+    default:
+        return BQD_ERR_INVALID_ARG;
+    }
+}
+
+extern "C" int64_t bqd_get_option(int option)
+{
+    switch (option) {
+    case BQD_OPT_KERNEL: return opt_kernel();
+    case BQD_OPT_T5_STAGES: return opt_t5_stages();
+    case BQD_OPT_DEBUG_PLAN: return opt_debug_plan() ? 1 : 0;
+    case BQD_OPT_WAIT_LIMIT_NS: return (int64_t)opt_wait_ns();
+    default: return -1;
+    }
 }

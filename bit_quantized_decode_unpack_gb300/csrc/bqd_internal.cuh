@@ -82,4 +82,12 @@ int take_qmv_t5r_timeouts(unsigned int *count);
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Process-wide options (bqd_set_option; first values from the environment,
+// read once).
+constexpr int64_t kDefaultWaitNs = 1000000000;  // a bounded wait gives up after 1 s
+int opt_kernel();         // BQD_KERNEL_*
+int opt_t5_stages();      // 0 = planner's choice, else 1 or 2 (register-streaming t5 kernel)
+bool opt_debug_plan();    // print each launch plan to stderr
+uint64_t opt_wait_ns();   // limit of the ring kernels' pipeline waits, ns
+
 }  // namespace bqd

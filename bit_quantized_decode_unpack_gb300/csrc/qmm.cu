@@ -785,7 +785,7 @@ int launch_qmm(const QmvArgs &a, cudaStream_t s)
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return BQD_ERR_CUDA;
-    if (getenv("BQD_DEBUG_PLAN"))
+    if (opt_debug_plan())
         fprintf(stderr, "bqd qmm plan: fmt=%d M=%d N=%d K=%d gs=%d -> bx=%d x%d tiles=%d S=%d gpr=%d stages=%d smem=%zu\n",
                 a.fmt, p.M, p.N, p.K, a.gs, p.bx, NH, tiles, S, p.gpr, p.stages, smem);
     if (a.fmt == BQD_FMT_T5) {

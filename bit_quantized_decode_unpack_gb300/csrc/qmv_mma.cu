@@ -677,7 +677,7 @@ int launch_qmv_mma(const QmvArgs &a, cudaStream_t s)
         p.x = a.x + m0 * a.K;
         p.out = a.out + m0 * a.N;
         p.S = pl.S; p.Tc = pl.Tc; p.Cs = pl.Cs;
-        if (getenv("BQD_DEBUG_PLAN"))
+        if (opt_debug_plan())
             fprintf(stderr, "bqd %s plan: N=%d K=%d M=%d gs=%d -> S=%d Tc=%d Cs=%d R=%d grid=%d smem=%zu\n", "mma",
                     p.N, p.K, M, a.gs, pl.S, pl.Tc, pl.Cs, pl.R, pl.R * pl.S, pl.smem);
         const int st = a.fmt == BQD_FMT_AFFINE2 ? launch_fmt<BQD_FMT_AFFINE2>(p, pl, a.biases != nullptr, s)

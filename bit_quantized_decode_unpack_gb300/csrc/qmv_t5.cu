@@ -434,9 +434,8 @@ bool make_plan(int gs, int M, int tiles, int chunks, int sms, OccFn occ, Plan &b
 {
     double best_cost = 1e30;
     bool found = false;
-    // testing knob: BQD_T5_STAGES=1|2 restricts the stage count
-    const char *knob = getenv("BQD_T5_STAGES");
-    const int ns_only = knob ? atoi(knob) : 0;
+    // testing option: the stage count restricted to 1 or 2 (bqd_set_option)
+    const int ns_only = opt_t5_stages();
     for (int NS = 2; NS >= 1; --NS) {
         if (ns_only && NS != ns_only) continue;
         for (int S = 1; S <= 8 && S <= chunks; ++S) {
@@ -567,7 +566,7 @@ int launch_qmv_t5(const QmvArgs &a, cudaStream_t s)
         p.x = a.x + m0 * a.K;
         p.out = a.out + m0 * a.N;
         p.S = pl.S; p.Tc = pl.Tc; p.Cs = pl.Cs; p.NS = pl.NS;
-        if (getenv("BQD_DEBUG_PLAN"))
+        if (opt_debug_plan())
             fprintf(stderr, "bqd %s plan: N=%d K=%d M=%d gs=%d -> S=%d Tc=%d Cs=%d R=%d NS=%d grid=%d smem=%zu\n", "t5",
                     p.N, p.K, M, a.gs, pl.S, pl.Tc, pl.Cs, pl.R, pl.NS, pl.R * pl.S, pl.smem);
         int st;

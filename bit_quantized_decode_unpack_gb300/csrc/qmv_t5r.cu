@@ -667,7 +667,7 @@ int launch_r(const T5RParams &p0, const CUtensorMap &wmap, cudaStream_t s)
     CUtensorMap xmap;
     if (!encode_2d(xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.x, p.K, p.Mtot, (int64_t)p.K * 2, 256, p.M))
         return BQD_ERR_CUDA;
-    if (getenv("BQD_DEBUG_PLAN"))
+    if (opt_debug_plan())
         fprintf(stderr, "bqd t5r plan: N=%d K=%d M=%d (%d per pass) gs=%d -> S=%d Cs=%d stages=%d R=%d grid=%dx%d smem=%zu\n",
                 p.N, p.K, p.Mtot, p.M, GS, pl.S, pl.Cs, pl.stages, pl.R, pl.R * pl.S, P, pl.smem);
     auto kern = qmv_t5r_kernel<GS, HAS_BIAS>;

@@ -779,7 +779,7 @@ int launch_t(const TmaParams &p0, const CUtensorMap &map, int chunks, cudaStream
     if (!encode_f16(smap, p.scales, p.G, p.N, pl.BX)) return BQD_ERR_CUDA;
     bmap = smap;
     if (HAS_BIAS && !encode_f16(bmap, p.biases, p.G, p.N, pl.BX)) return BQD_ERR_CUDA;
-    if (getenv("BQD_DEBUG_PLAN"))
+    if (opt_debug_plan())
         fprintf(stderr, "bqd tma plan: N=%d K=%d M=%d gs=%d -> S=%d Cs=%d stages=%d R=%d BX=%d grid=%dx%d smem=%zu\n",
                 p.N, p.K, p.M, GS, pl.S, pl.Cs, pl.stages, pl.R, pl.BX, pl.R * pl.S, P, pl.smem);
     auto kern = qmv_tma_kernel<FMT, GS, HAS_BIAS, MP>;

@@ -212,6 +212,33 @@ int bqd_spec_decode_verify(const void *logits, int dtype, const int32_t *draft, 
  */
 int bqd_device_status(bqd_stream_t stream);
 
+/*
+ * Process-wide options: a control for tests and measurements, with no
+ * counterpart on the page.  Host-only; a change applies to calls made after
+ * it (calls already enqueued keep what they were launched with).
+ *   BQD_OPT_KERNEL         BQD_KERNEL_AUTO (the dispatcher picks) or one
+ *                          kernel family forced for every QMV call; a forced
+ *                          family that cannot serve a request makes that call
+ *                          return BQD_ERR_UNSUPPORTED instead of falling back
+ *   BQD_OPT_T5_STAGES      0, or 1 / 2: the ring depth of the register-
+ *                          streaming t5 kernel (0 = the planner's choice)
+ *   BQD_OPT_WAIT_LIMIT_NS  time, in ns of %globaltimer, after which a pipeline
+ *                          wait of the ring kernels gives up (see
+ *                          bqd_device_status); 0 restores the default of 1 s.
+ *                          The waits that let a CTA's own copies land before
+ *                          it exits always keep the default limit
+ *   BQD_OPT_DEBUG_PLAN     non-zero: print each launch plan to stderr
+ * The environment gives the first values, read once on first use:
+ * BQD_FORCE_KERNEL=generic|mma|tma|qmm, BQD_T5_STAGES=1|2, BQD_DEBUG_PLAN.
+ * bqd_set_option returns BQD_OK or BQD_ERR_INVALID_ARG (unknown option or
+ * value out of range); bqd_get_option returns the value, or -1 for an
+ * unknown option.
+ */
+enum { BQD_OPT_KERNEL = 1, BQD_OPT_T5_STAGES = 2, BQD_OPT_WAIT_LIMIT_NS = 3, BQD_OPT_DEBUG_PLAN = 4 };
+enum { BQD_KERNEL_AUTO = 0, BQD_KERNEL_GENERIC = 1, BQD_KERNEL_MMA = 2, BQD_KERNEL_TMA = 3, BQD_KERNEL_QMM = 4 };
+int bqd_set_option(int option, int64_t value);
+int64_t bqd_get_option(int option);
+
 #ifdef __cplusplus
 }
 #endif

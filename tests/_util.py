@@ -2,7 +2,6 @@
 from __future__ import annotations
 
 import contextlib
-import os
 
 import numpy as np
 
@@ -26,18 +25,14 @@ def assert_within_tolerance(y_gpu, y_ref, bound, what=""):
 
 @contextlib.contextmanager
 def forced_kernel(name):
-    old = os.environ.get("BQD_FORCE_KERNEL")
-    if name is None:
-        os.environ.pop("BQD_FORCE_KERNEL", None)
-    else:
-        os.environ["BQD_FORCE_KERNEL"] = name
+    """Force one kernel family (bqd_set_option) for the duration of a block."""
+    import bit_quantized_decode_unpack_gb300 as bqd
+    old = bqd.get_option(bqd.OPT_KERNEL)
+    bqd.force_kernel(name)
     try:
         yield
     finally:
-        if old is None:
-            os.environ.pop("BQD_FORCE_KERNEL", None)
-        else:
-            os.environ["BQD_FORCE_KERNEL"] = old
+        bqd.set_option(bqd.OPT_KERNEL, old)
 
 
 def to_dev(a, dev="cuda"):

@@ -46,5 +46,8 @@ def test_reference_arm_other_ranks_print_nothing():
 
 
 def test_bench_reads_nothing_from_outside_the_repository():
+    """bench.py names no absolute path: every file it reads is found relative
+    to the repository (the measured peaks, the profiles, the oracle)."""
+    import re
     text = (ROOT / "bench.py").read_text()
-    assert "/root/reference" not in text and "reference/PAPER" not in text
+    assert not re.findall(r"""["']/[A-Za-z]""", text)

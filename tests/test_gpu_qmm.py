@@ -1,7 +1,7 @@
 """GPU parity of the prefill matrix product (tcgen05 tensor cores; the
 dispatcher's choice for large M) against the float64 oracle, through the C
 ABI: t5 and the 1/2-bit formats.  Most cases force the product
-(BQD_FORCE_KERNEL=qmm) so that it is tested at every shape.
+(the kernel option set to "qmm") so that it is tested at every shape.
 
 Page: "oMLX Bonsai 自定义内核:Qwen 系列快速 QMV 路径完整解析" §二.3 -- for M > 16
 the t5 weights go through a fused unpack + matrix-multiply kernel; §二.1 -- the
@@ -159,7 +159,7 @@ def test_t5_gs64_two_column_blocks_per_cta(bias):
 @pytest.mark.parametrize("fmt", [F1, F2, T5])
 @pytest.mark.parametrize("gs", [64, 128])
 def test_forced_product_at_decode_sizes(fmt, gs):
-    """BQD_FORCE_KERNEL=qmm runs the product for M <= 16 too (one x tile of 32
+    """The forced product runs for M <= 16 too (one x tile of 32
     columns, mostly empty): still exact to the bar."""
     for M, N, K in [(1, 129, 1024), (5, 256, 2048), (16, 40, 1024)]:
         run(synth.problem(fmt, M, N, K, gs, sym=fmt == T5), "qmm")

@@ -67,7 +67,7 @@ MMA_SHAPES = [(1, 17, 1024), (2, 300, 2048), (3, 130, 3072), (5, 1000, 1024), (8
 @pytest.mark.parametrize("gs", [64, 128])
 @pytest.mark.parametrize("sym", [False, True])
 def test_tensor_core_paths_forced(kernel, fmt, gs, sym):
-    """BQD_FORCE_KERNEL=mma|tma makes an unsupported request an error instead
+    """A forced kernel family makes an unsupported request an error instead
     of a fallback, so these cases are known to run on the named kernel."""
     for M, N, K in MMA_SHAPES:
         p = synth.problem(fmt, M, N, K, gs, sym=sym)
@@ -142,11 +142,14 @@ def test_zero_codes_zero_bias_give_exact_zeros(kernel, fmt):
 
 @pytest.mark.parametrize("stages", ["1", "2"])
 @pytest.mark.parametrize("gs", [64, 128])
-def test_t5_stage_ring_depths(stages, gs, monkeypatch):
+def test_t5_stage_ring_depths(stages, gs):
     """The t5 kernel's weight ring with one and with two stages per warp."""
-    monkeypatch.setenv("BQD_T5_STAGES", stages)
-    for M, N, K in [(1, 300, 3072), (5, 1000, 2048), (8, 40, 5120)]:
-        run_case(synth.problem(T5, M, N, K, gs, sym=True), "mma")
+    bqd.set_option(bqd.OPT_T5_STAGES, int(stages))
+    try:
+        for M, N, K in [(1, 300, 3072), (5, 1000, 2048), (8, 40, 5120)]:
+            run_case(synth.problem(T5, M, N, K, gs, sym=True), "mma")
+    finally:
+        bqd.set_option(bqd.OPT_T5_STAGES, 0)
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
