@@ -235,7 +235,13 @@ int bqd_device_status(bqd_stream_t stream);
  * unknown option.
  */
 enum { BQD_OPT_KERNEL = 1, BQD_OPT_T5_STAGES = 2, BQD_OPT_WAIT_LIMIT_NS = 3, BQD_OPT_DEBUG_PLAN = 4 };
-enum { BQD_KERNEL_AUTO = 0, BQD_KERNEL_GENERIC = 1, BQD_KERNEL_MMA = 2, BQD_KERNEL_TMA = 3, BQD_KERNEL_QMM = 4 };
+enum {
+    BQD_KERNEL_AUTO = 0,    /* the dispatcher's choice                       */
+    BQD_KERNEL_GENERIC = 1, /* CUDA-core kernel, any shape                   */
+    BQD_KERNEL_MMA = 2,     /* register-streaming tensor-core decode kernels */
+    BQD_KERNEL_TMA = 3,     /* TMA-ring decode kernels                       */
+    BQD_KERNEL_QMM = 4      /* tcgen05 prefill product                       */
+};
 int bqd_set_option(int option, int64_t value);
 int64_t bqd_get_option(int option);
 
