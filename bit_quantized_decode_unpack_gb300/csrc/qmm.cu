@@ -66,12 +66,10 @@ constexpr int kLutCopiesQ = 16;              // lane l reads copy l % 16: fewer 
 
 __device__ unsigned int g_qmm_timeouts = 0;
 
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity)
+// pipeline waits give up after the call's limit; drain waits after a second
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, unsigned long long limit_ns)
 {
-    for (uint32_t i = 0; i < kWaitSpins; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    atomicAdd(&g_qmm_timeouts, 1u);
-    return false;
+    return mbar_wait_for(bar, parity, limit_ns, &g_qmm_timeouts);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
@@ -175,6 +173,7 @@ struct QmmParams {
     long long row_bytes;
     int bx, S, gpr, stages;  // gpr: K groups per cluster rank
     uint32_t zero;           // always 0: keeps the magic constants in registers
+    unsigned long long wait_ns;  // limit of the pipeline waits
 };
 
 // byte offset of 16-byte chunk c of row r inside one 128-row x 64-code
@@ -258,7 +257,7 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
             int issued = 0, s = 0;
             uint32_t rpar = 1;  // parity of empty_bar[s] that frees it for step it (>= NST)
             for (int it = 0; it < steps; ++it) {
-                if (it >= NST && !wait_bounded(smem_addr(&empty_bar[s]), rpar)) {
+                if (it >= NST && !wait_bounded(smem_addr(&empty_bar[s]), rpar, p.wait_ns)) {
                     abort_flag = 1;
                     break;
                 }
@@ -277,11 +276,12 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
                     rpar ^= 1u;
                 }
             }
-            if (abort_flag) {
-                // drain the copies this CTA issued (bounded) before anyone leaves
-                for (int it = max(0, issued - NST); it < issued; ++it)
-                    wait_bounded(smem_addr(&x_full[it % NST]), (it / NST) & 1);
-            }
+            // every copy this CTA issued lands before anyone leaves, whether or
+            // not the MMA issuer consumed it (it stops early once a wait of its
+            // expires, possibly after this loop has ended).  Each slot's last
+            // phase is the one waited for, so the parity is unambiguous.
+            for (int it = max(0, issued - NST); it < issued; ++it)
+                wait_bounded(smem_addr(&x_full[it % NST]), (it / NST) & 1, kDrainWaitNs);
         }
     } else if (warp == kMmaWarpQ) {
         // ---- MMA issuer -----------------------------------------------------------
@@ -291,7 +291,7 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
             int s = 0;
             uint32_t par = 0;
             for (int it = 0; it < steps; ++it) {
-                ok = wait_bounded(smem_addr(&x_full[s]), par) && wait_bounded(smem_addr(&a_full[s]), par);
+                ok = wait_bounded(smem_addr(&x_full[s]), par, p.wait_ns) && wait_bounded(smem_addr(&a_full[s]), par, p.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t a0 = smem_addr(smem + (size_t)s * stage_bytes);
@@ -405,7 +405,7 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
         // one K step after its data is in registers: wait for the stage, decode,
         // store the A tile, arrive; false once a bounded wait has expired
         auto step_body = [&](int it, const uint32_t (&cur)[HW], uint16_t sb, uint16_t bb) -> bool {
-            if (it >= NST && !wait_bounded(smem_addr(&empty_bar[s]), rpar)) {
+            if (it >= NST && !wait_bounded(smem_addr(&empty_bar[s]), rpar, p.wait_ns)) {
                 abort_flag = 1;
                 return false;
             }
@@ -607,7 +607,8 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
 
     // ---- epilogue: warp w drains TMEM lanes 32 (w % 4) .. +31, column half w / 4 ------
     __syncthreads();
-    if (warp < kDecodeWarpsQ && steps > 0) wait_bounded(smem_addr(&done_bar), 0);
+    // every issued MMA has completed before TMEM is read or freed
+    if (warp < kDecodeWarpsQ && steps > 0) wait_bounded(smem_addr(&done_bar), 0, kDrainWaitNs);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -749,6 +750,7 @@ int launch_qmm(const QmvArgs &a, cudaStream_t s)
     p.w = a.w; p.scales = a.scales; p.biases = a.biases; p.out = a.out; p.ratio = a.ratio;
     p.M = (int)a.M; p.N = (int)a.N; p.K = (int)a.K; p.G = (int)a.G;
     p.row_bytes = a.row_bytes;
+    p.wait_ns = (unsigned long long)opt_wait_ns();
     p.zero = 0;
     p.bx = a.M <= 32 ? 32 : (a.M <= 64 ? 64 : (a.M <= 128 ? 128 : 256));
     // 1/2-bit (and t5 at gs=64) with more than 256 x rows on a wide layer: two

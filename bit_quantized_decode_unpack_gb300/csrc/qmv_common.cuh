@@ -132,7 +132,57 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 // async-proxy (bulk copy) writes to it
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-constexpr uint32_t kWaitSpins = 1u << 22;  // ~ a second of try_wait round trips
+// ---- bounded waits ----------------------------------------------------------------
+
+__device__ __forceinline__ unsigned long long globaltimer_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// non-blocking probe of a phase (never suspends the thread)
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of parity `parity` of the mbarrier at `bar`; give up
+// once `limit_ns` of %globaltimer have passed, counting the expiry in *expired.
+// Limits of at least 20 us probe with try_wait (which may suspend the thread
+// for a while) and read the clock every 64 probes; shorter ones spin on
+// test_wait (a try_wait may sleep until the phase completes, which would hide
+// a short limit).
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, unsigned long long limit_ns,
+                                              unsigned int *expired)
+{
+    if (limit_ns >= 20000ull) {
+        if (mbar_try_wait(bar, parity)) return true;
+        const unsigned long long t0 = globaltimer_ns();
+        while (true) {
+            for (int i = 0; i < 64; ++i)
+                if (mbar_try_wait(bar, parity)) return true;
+            if (globaltimer_ns() - t0 >= limit_ns) break;
+        }
+    } else {
+        if (mbar_test_wait(bar, parity)) return true;
+        const unsigned long long t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < limit_ns)
+            if (mbar_test_wait(bar, parity)) return true;
+    }
+    atomicAdd(expired, 1u);
+    return false;
+}
+
+// limit of the waits that let a CTA's own copies (and MMAs) finish before it
+// leaves: they always keep the full second
+constexpr unsigned long long kDrainWaitNs = 1000000000ull;
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
 {

@@ -47,10 +47,7 @@ __device__ unsigned int g_qmv_mma_timeouts = 0;
 // Bounded wait: false (and the timeout counter bumped) if the phase never completes.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
 {
-    for (uint32_t i = 0; i < kWaitSpins; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    atomicAdd(&g_qmv_mma_timeouts, 1u);
-    return false;
+    return mbar_wait_for(bar, parity, kDrainWaitNs, &g_qmv_mma_timeouts);
 }
 
 constexpr int kThreads = kWarps * 32;

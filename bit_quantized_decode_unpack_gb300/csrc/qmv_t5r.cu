@@ -68,6 +68,7 @@ struct T5RParams {
     int N, K, G, chunks, S, Cs, stages, RS;
     uint32_t stage_bytes;
     uint32_t zero;  // always 0: keeps the magic constants opaque (in registers)
+    unsigned long long wait_ns;  // limit of the pipeline waits
 };
 
 template <int GS>
@@ -103,12 +104,10 @@ struct Stage5 {
     __host__ __device__ static constexpr int bytes(int M) { return (sx_off(M) + G5<GS>::NB * M * 32 + 127) / 128 * 128; }
 };
 
-__device__ __forceinline__ bool wait_bounded_r(uint32_t bar, uint32_t parity)
+// pipeline waits give up after the call's limit; drain waits after a second
+__device__ __forceinline__ bool wait_bounded_r(uint32_t bar, uint32_t parity, unsigned long long limit_ns)
 {
-    for (uint32_t i = 0; i < kWaitSpins; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    atomicAdd(&g_qmv_t5r_timeouts, 1u);
-    return false;
+    return mbar_wait_for(bar, parity, limit_ns, &g_qmv_t5r_timeouts);
 }
 
 __device__ __forceinline__ void mbar_arrive_r(uint32_t bar)
@@ -261,14 +260,14 @@ __global__ void __launch_bounds__(kThreadsR, 2)
         for (int it = 0; it < ncl; ++it) {
             const uint32_t st = ring_a + (uint32_t)s * STB;
             if (it >= NST) {
-                bool ok = lane == 0 ? wait_bounded_r(smem_addr(&empty_bar[s]), par ^ 1u) : true;
+                bool ok = lane == 0 ? wait_bounded_r(smem_addr(&empty_bar[s]), par ^ 1u, p.wait_ns) : true;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
                 issue(it, s);
                 issued_w = it + 1;
             }
             {
-                bool ok = lane == 0 ? wait_bounded_r(smem_addr(&x_bar[it & 1]), (it >> 1) & 1) : true;
+                bool ok = lane == 0 ? wait_bounded_r(smem_addr(&x_bar[it & 1]), (it >> 1) & 1, p.wait_ns) : true;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
             }
@@ -356,8 +355,8 @@ __global__ void __launch_bounds__(kThreadsR, 2)
         for (int it = done; it < issued_w; ++it) mbar_arrive_r(smem_addr(&full_bar[it % NST]));
         if (lane == 0) {
             for (int it = max(0, issued_w - NST); it < issued_w; ++it)
-                wait_bounded_r(smem_addr(&full_bar[it % NST]), (it / NST) & 1);
-            if (done < ncl) wait_bounded_r(smem_addr(&x_bar[done & 1]), (done >> 1) & 1);
+                wait_bounded_r(smem_addr(&full_bar[it % NST]), (it / NST) & 1, kDrainWaitNs);
+            if (done < ncl) wait_bounded_r(smem_addr(&x_bar[done & 1]), (done >> 1) & 1, kDrainWaitNs);
         }
         __syncwarp();
         if (S > 1) {
@@ -380,7 +379,7 @@ __global__ void __launch_bounds__(kThreadsR, 2)
     int s = 0;
     uint32_t par = 0;
     for (int it = 0; it < ncl; ++it) {
-        if (!wait_bounded_r(smem_addr(&full_bar[s]), par)) break;
+        if (!wait_bounded_r(smem_addr(&full_bar[s]), par, p.wait_ns)) break;
         // this lane's 52-byte slices of rows r0 and r0+8
         uint32_t wa[13], wb[13];
 #pragma unroll
@@ -731,6 +730,7 @@ int launch_qmv_t5r(const QmvArgs &a, cudaStream_t s)
     p.N = (int)a.N; p.K = (int)a.K; p.G = (int)a.G;
     p.chunks = (int)(a.K / kCodesR);
     p.zero = 0;
+    p.wait_ns = (unsigned long long)opt_wait_ns();
     p.S = p.Cs = p.stages = p.RS = 0;
     p.stage_bytes = 0;
     const bool hb = a.biases != nullptr;

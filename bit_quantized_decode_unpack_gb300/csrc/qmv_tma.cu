@@ -66,16 +66,15 @@ struct TmaParams {
     float ratio;
     int M, N, K, G, chunks, S, Cs, stages, RS, BX;
     uint32_t zero;  // always 0: keeps the magic constants opaque (in registers)
+    unsigned long long wait_ns;  // limit of the pipeline waits
 };
 
 // ---- PTX wrappers local to this kernel ---------------------------------------
 
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity)
+// pipeline waits give up after the call's limit; drain waits after a second
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, unsigned long long limit_ns)
 {
-    for (uint32_t i = 0; i < kWaitSpins; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    atomicAdd(&g_qmv_tma_timeouts, 1u);
-    return false;
+    return mbar_wait_for(bar, parity, limit_ns, &g_qmv_tma_timeouts);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
@@ -273,7 +272,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         for (int it = 0; it < ncl; ++it) {
             const uint32_t st = ring_a + (uint32_t)s * SL::kBytes;
             if (it >= NST) {
-                bool ok = lane == 0 ? wait_bounded(smem_addr(&empty_bar[s]), par ^ 1u) : true;
+                bool ok = lane == 0 ? wait_bounded(smem_addr(&empty_bar[s]), par ^ 1u, p.wait_ns) : true;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
                 issue_weights(it, s);
@@ -368,8 +367,8 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         // issued stage was also prepared, so its barrier can complete)
         if (lane == 0) {
             for (int it = max(0, done - NST); it < done; ++it)
-                wait_bounded(smem_addr(&full_bar[it % NST]), (it / NST) & 1);
-            if (ncl > 0) wait_bounded(smem_addr(&sc_bar), 0);
+                wait_bounded(smem_addr(&full_bar[it % NST]), (it / NST) & 1, kDrainWaitNs);
+            if (ncl > 0) wait_bounded(smem_addr(&sc_bar), 0, kDrainWaitNs);
         }
         __syncwarp();
         if (S > 1) {
@@ -400,9 +399,9 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     uint32_t st_a = ring_a;
     int s = 0;
     uint32_t par = 0;
-    const bool sc_ok = ncl == 0 || wait_bounded(smem_addr(&sc_bar), 0);
+    const bool sc_ok = ncl == 0 || wait_bounded(smem_addr(&sc_bar), 0, p.wait_ns);
     for (int it = 0; it < ncl && sc_ok; ++it) {
-        if (!wait_bounded(smem_addr(&full_bar[s]), par)) break;
+        if (!wait_bounded(smem_addr(&full_bar[s]), par, p.wait_ns)) break;
         // scales of the four rows for the chunk's groups
         uint32_t sw[4][GPC / 2];
 #pragma unroll
@@ -737,6 +736,7 @@ int launch_qmv_tma(const QmvArgs &a, cudaStream_t s)
     p.N = (int)a.N; p.K = (int)a.K; p.G = (int)a.G;
     p.chunks = (int)(a.K / kChunkT);
     p.zero = 0;
+    p.wait_ns = (unsigned long long)opt_wait_ns();
     p.S = p.Cs = p.stages = p.RS = 0;
     const bool hb = a.biases != nullptr;
     // M <= 8: one pass with 4 or 8 B-fragment columns; larger M: passes of 8

@@ -150,3 +150,28 @@ def test_spec_decode_verify_validates_on_host(lib):
     assert call(lg=0x1002, dt=2) == ALIGN  # fp32 logits need 4-byte alignment
     assert call(a=0x3002) == ALIGN
     assert call(B=0, lg=None, dr=None, a=None, n=None) == 0
+
+
+def test_options_set_get_and_validate(lib):
+    """bqd_set_option / bqd_get_option: process-wide controls for tests and
+    measurements, validated on the host."""
+    INV = 1
+    old = {o: lib.bqd_get_option(o) for o in (1, 2, 3, 4)}
+    try:
+        for k in (0, 1, 2, 3, 4):
+            assert lib.bqd_set_option(1, k) == 0 and lib.bqd_get_option(1) == k
+        assert lib.bqd_set_option(1, 5) == INV and lib.bqd_set_option(1, -1) == INV
+        assert lib.bqd_set_option(2, 2) == 0 and lib.bqd_get_option(2) == 2
+        assert lib.bqd_set_option(2, 3) == INV
+        assert lib.bqd_set_option(3, 250) == 0 and lib.bqd_get_option(3) == 250
+        assert lib.bqd_set_option(3, 0) == 0 and lib.bqd_get_option(3) == 1_000_000_000  # default restored
+        assert lib.bqd_set_option(3, -5) == INV
+        assert lib.bqd_set_option(99, 1) == INV and lib.bqd_get_option(99) == -1
+        # the binding's names map onto the same values
+        bqd.force_kernel("qmm")
+        assert lib.bqd_get_option(bqd.OPT_KERNEL) == bqd.KERNELS["qmm"]
+        bqd.force_kernel(None)
+        assert lib.bqd_get_option(bqd.OPT_KERNEL) == 0
+    finally:
+        for o, v in old.items():
+            lib.bqd_set_option(o, v)
