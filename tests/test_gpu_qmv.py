@@ -79,10 +79,12 @@ def test_tensor_core_paths_forced(kernel, fmt, gs, sym):
 # TMA-ring kernel: its envelope is K a multiple of 256 with K/gs a multiple of
 # 8 (16-byte scale rows); shapes span row blocks of 256 with ragged tails,
 # split-K clusters of many sizes (portable and not), M up to 8 in one pass and
-# passes of 8 rows (grid rows of one launch) beyond, the last one ragged
+# passes of 8 rows (grid rows of one launch) beyond (every M from 9 to 16,
+# and 27 and 33), the last one ragged
 TMA_SHAPES = [(1, 1, 1024), (2, 127, 1024), (3, 256, 2048), (4, 257, 3072), (5, 383, 4096), (7, 1024, 5120),
               (8, 2000, 1024), (9, 200, 2048), (16, 130, 1024), (1, 5120, 17408), (5, 300, 17408), (2, 4096, 6144),
-              (27, 300, 2048)]
+              (27, 300, 2048), (6, 70, 1024), (10, 513, 2048), (11, 64, 5120), (12, 300, 3072), (13, 257, 1024),
+              (14, 1000, 2048), (15, 33, 4096), (33, 129, 1024)]
 
 
 @pytest.mark.parametrize("fmt", [F1, F2])
@@ -318,3 +320,16 @@ def test_non_default_stream():
     packed = oracle.c_pack(p["codes"], T5, 128)
     yr, bound = oracle.c_qmv_rows(p["x"], packed, p["scales"], None, T5, 128)
     assert_within_tolerance(y.cpu().numpy(), yr, bound)
+
+
+MID_M = [(F2, M, N, K, gs) for M in (9, 12, 16) for (N, K) in [(17408, 5120), (5120, 17408)] for gs in (64, 128)]
+MID_M += [(F1, M, 17408, 5120, 64) for M in (10, 16)]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("fmt,M,N,K,gs", MID_M)
+def test_mid_m_one_pass_full_size_sampled_rows(fmt, M, N, K, gs):
+    """9 <= M <= 16 (two passes of x rows in one launch of the decode kernel)
+    at the layer sizes, on sampled rows (the dispatcher's choice there)."""
+    p = synth.problem(fmt, M, N, K, gs)
+    run_case(p, None, rows=_sample_rows(N, seed=N + M))
