@@ -527,8 +527,9 @@ def time_spec_verify(dev, reps: int = 20):
 
 
 def kernel_traffic_from_profiles():
-    """DRAM-bytes / algorithmic-bytes ratio of the QMV kernels from the committed
-    ncu summaries, or None when a kernel source changed since it was taken."""
+    """DRAM-bytes / algorithmic-bytes ratio of the QMV kernels over the eight
+    calls of one sweep group, captured without cache flushes between them
+    (profiles/qmv_traffic.json), or None when a kernel source changed since."""
     p = ROOT / "profiles" / "qmv_traffic.json"
     if not p.exists():
         return None
@@ -537,8 +538,7 @@ def kernel_traffic_from_profiles():
         for src, digest in d["kernel_sha256"].items():
             if hashlib.sha256((ROOT / src).read_bytes()).hexdigest() != digest:
                 return None
-        ratios = list(d["dram_over_algorithmic"].values())
-        return sum(ratios) / len(ratios)
+        return float(d["aggregate"])
     except Exception:
         return None
 
@@ -578,6 +578,52 @@ def run_case(spec: str, sets: int, reps: int = 64):
     nb = call_bytes(fmt, sym or fmt == T5, M, N, K, gs)
     print(json.dumps({"case": spec, "us_per_call_eager": us, "gbs": nb / (us * 1e-6) / 1e9,
                       "tflops": 2.0 * M * N * K / (us * 1e-6) / 1e12}), flush=True)
+    return 0
+
+
+def run_group(spec: str):
+    """--group M,proj: the eight calls of one (M, projection) group of the
+    sweep (4 variants x 2 group sizes), in sweep order, each on tensors of its
+    own, after a 512 MB read of a buffer not written since it was allocated:
+    the L2 then holds only clean lines of that buffer, so no write-back of
+    earlier dirty lines lands inside a captured launch.  Used for the ncu
+    check that a step's calls read their weights from DRAM, not from the L2
+    (with --cache-control none, DRAM bytes per launch = algorithmic bytes)."""
+    import torch
+    import bit_quantized_decode_unpack_gb300 as bqd
+    from bit_quantized_decode_unpack_gb300 import _build, synth
+    _build.build()
+    M_s, proj = spec.split(",")
+    M = int(M_s)
+    N, K = dict(shapes())[proj]
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3)
+    calls = [c for c in sweep_calls() if c["M"] == M and c["proj"] == proj]
+    data = []
+    for c in calls:
+        s_ = synth.torch_scales(gen, N, K // c["gs"], dev)
+        b_ = None if c["sym"] else synth.torch_biases(gen, c["fmt"], s_, dev)
+        w = bqd.pack(synth.torch_codes(gen, c["fmt"], N, K, dev), c["fmt"], c["gs"])
+        x = synth.torch_activations(gen, M, K, dev)
+        data.append((c, x, w, s_, b_, torch.empty(M, N, dtype=torch.float16, device=dev)))
+    flush = torch.ones(128 * 2**20, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    rows = []
+    for rep in range(3):
+        flush.sum()
+        torch.cuda.synchronize()
+        for c, x, w, s_, b_, y in data:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            bqd.qmv(x, w, s_, b_, c["fmt"], c["gs"], out=y)
+            e1.record()
+            e1.synchronize()
+            if rep == 2:
+                nb = call_bytes(c["fmt"], c["sym"], M, N, K, c["gs"])
+                rows.append({"variant": c["variant"], "gs": c["gs"], "bytes": nb,
+                             "us_eager": round(e0.elapsed_time(e1) * 1e3, 2)})
+    print(json.dumps({"group": spec, "calls": rows}), flush=True)
     return 0
 
 
@@ -697,12 +743,16 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=120.0,
                     help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--case", type=str, default=None, help="fmt,M,N,K,gs[,sym]: time one configuration")
+    ap.add_argument("--group", type=str, default=None,
+                    help="M,proj: the eight calls of one sweep group on their own tensors (L2 check)")
     ap.add_argument("--spec-case", type=str, default=None,
                     help="B,D,V: time the speculative-decoding verification on fp16 logits")
     args = ap.parse_args()
 
     if args.case:
         return run_case(args.case, args.sets)
+    if args.group:
+        return run_group(args.group)
     if args.spec_case:
         import torch
         global SPEC_CASE
@@ -774,8 +824,9 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_source": src,
                          "traffic": None if tr is None else tr * sweep.bytes_per_step,
-                         "traffic_basis": "dram bytes / algorithmic bytes of single-launch ncu captures "
-                                          "(profiles/qmv_traffic.json) x bytes per step",
+                         "traffic_basis": "DRAM bytes / algorithmic bytes over the eight calls of one sweep "
+                                          "group, no cache flush between them (profiles/qmv_traffic.json), "
+                                          "x bytes per step",
                          "kernel": "qmv (all 280 launches of a step)",
                          "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS},
             "e2e": {"value": value_e2e, "unit": UNIT, "h2d_bytes_per_step": sweep.h2d,

@@ -75,17 +75,6 @@ template <int GS> struct TF<BQD_FMT_AFFINE2, GS> {
         base = 64 * P + 16 * tslot;
         pp0 = 2 * P;
     }
-    // Sub-unit u of group j = the 8 registers (four MMAs) of one word:
-    // word j*(GS/64) + u of the thread's words.
-    static constexpr int kSub = GS / 64;
-    __host__ __device__ static constexpr int sub_word(int j, int u) { return j * (GS / 64) + u; }
-    // x item k (of GS/64) of group j, quad slot t (inverse of xitem)
-    __host__ __device__ static constexpr int item_of(int j, int t, int k) { return 4 * (j * (GS / 64) + k) + t; }
-    template <int U>
-    __device__ static __forceinline__ void unpack_sub(uint32_t w, int t, const uint32_t (&mg)[10], uint32_t (&A)[8])
-    {
-        unpack_word(w, mg, A);
-    }
 };
 
 // 1-bit: 32 codes per word, pair i = (code i, code i+16).  A chunk is 32
@@ -148,26 +137,6 @@ template <int GS> struct TF<BQD_FMT_AFFINE1, GS> {
             tslot = (i >> 1) & 3;
             base = 32 * (4 * j + tslot) + 8 * u;
             pp0 = 4 * j + 2 * u;
-        }
-    }
-    // Sub-unit u of group j = 8 registers (four MMAs), all from the group's
-    // one word of the thread: gs=64 registers 0..7 of w >> 8(t&1); gs=128
-    // registers 0..7 (u = 0) or 8..15 (u = 1) of unpack_group.
-    static constexpr int kSub = GS / 64;
-    __host__ __device__ static constexpr int sub_word(int j, int u) { return j; }
-    // x item k (of GS/64) of group j, quad slot t (inverse of xitem)
-    __host__ __device__ static constexpr int item_of(int j, int t, int k) { return GS == 64 ? 4 * j + t : 8 * j + 2 * t + k; }
-    template <int U>
-    __device__ static __forceinline__ void unpack_sub(uint32_t w, int t, const uint32_t (&mg)[10], uint32_t (&A)[8])
-    {
-        if constexpr (GS == 64) {
-            unpack_from<8>(w >> (8 * (t & 1)), mg, &A[0]);
-        } else if constexpr (U == 0) {
-            unpack_from<8>(w, mg, &A[0]);
-        } else {
-            A[0] = and_or<(0x00010001u << 8)>(w, mg[8]);
-            A[1] = and_or<(0x00010001u << 9)>(w, mg[9]);
-            unpack_from<6>(w >> 10, mg, &A[2]);
         }
     }
 };

@@ -97,11 +97,15 @@ def test_tma_kernel_shapes(fmt, gs, sym):
         run_case(p, "tma")
 
 
-# t5 TMA-ring kernel: K a multiple of 1024; ragged 128-row blocks, split-K
-# clusters, passes of at most 5 x rows (grid rows of one launch; M = 6, 7, 12,
-# 16, 23 take several, the last one ragged)
-T5R_SHAPES = [(1, 1, 1024), (2, 127, 1024), (3, 129, 2048), (4, 300, 3072), (5, 1000, 5120), (6, 383, 4096),
-              (7, 260, 2048), (12, 64, 1024), (16, 130, 2048), (1, 5120, 17408), (5, 200, 17408), (23, 129, 2048)]
+# t5 TMA-ring kernel: K a multiple of 1024; ragged 128-row blocks (narrow
+# layers) and 256-row blocks (4353 x 5120, 4100 x 17408, 5120 x 17408), split-K
+# clusters, the column split (M <= 2) and the scaled path (M >= 3), passes of
+# at most 8 x rows (grid rows of one launch; M = 12, 16, 23 take several, the
+# last one ragged)
+T5R_SHAPES = [(1, 1, 1024), (2, 127, 1024), (2, 255, 1024), (3, 129, 2048), (3, 257, 2048), (4, 300, 3072),
+              (4, 513, 1024), (5, 1000, 5120), (6, 383, 4096), (6, 511, 3072), (7, 260, 2048), (12, 64, 1024),
+              (16, 130, 2048), (1, 5120, 17408), (5, 200, 17408), (23, 129, 2048), (1, 4353, 5120),
+              (2, 4100, 17408), (3, 4353, 5120), (8, 4100, 17408)]
 
 
 @pytest.mark.parametrize("gs", [64, 128])
@@ -126,10 +130,11 @@ def test_tma_envelope_and_fallback(fmt):
 
 
 @pytest.mark.parametrize("kernel", ["tma", "mma", "generic"])
-@pytest.mark.parametrize("fmt", [F1, F2])
+@pytest.mark.parametrize("fmt", [F1, F2, T5])
 def test_zero_codes_zero_bias_give_exact_zeros(kernel, fmt):
-    """w = s*0 + 0 everywhere: y is exactly 0 whatever x and s are (the TMA
-    kernel's offset cancellation is exact for code-free groups)."""
+    """w = s*0 + 0 everywhere: y is exactly 0 whatever x and s are (the ring
+    kernels' offset cancellation is exact for code-free groups: the offset
+    sums come from the same MMA sequence as the weights' products)."""
     import torch
     M, N, K, gs = 5, 300, 2048, 64
     p = synth.problem(fmt, M, N, K, gs)
