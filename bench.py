@@ -429,6 +429,44 @@ def config_tables(sweep, sweep_rows):
     return out
 
 
+MID_M = (9, 12, 16)
+
+
+def mid_m_table(sweep, reps: int = 3):
+    """Mid-M calls, between the decode kernels' M = 2~5 (p1 §二.2) and the t5
+    prefill product's M > 16 (p1 §二.3): the gate and down projections, 2-bit
+    gs=64 with biases and t5 gs=128, at M = 9, 12, 16.  µs per call as the
+    dispatcher runs it, and with the decode kernel (passes of 8 x rows as grid
+    rows of one launch) and the prefill product forced, over the sweep's
+    rotating weight sets."""
+    torch = sweep.torch
+    bqd = sweep.bqd
+    from bit_quantized_decode_unpack_gb300 import synth
+    gen = torch.Generator(device=sweep.dev)
+    gen.manual_seed(7)
+    rows = []
+    old = bqd.get_option(bqd.OPT_KERNEL)
+    try:
+        for proj in ("gate_proj", "down_proj"):
+            N, K = dict(shapes())[proj]
+            for variant, fmt, sym, gs in (("affine2", F2, False, 64), ("t5", T5, True, 128)):
+                for M in MID_M:
+                    c = dict(M=M, proj=proj, N=N, K=K, variant=variant, fmt=fmt, sym=sym, gs=gs)
+                    x = synth.torch_activations(gen, M, K, sweep.dev)
+                    y = torch.empty((M, N), dtype=torch.float16, device=sweep.dev)
+                    r = dict(proj=proj, variant=variant, gs=gs, M=M)
+                    for key, kern in (("us", None), ("us_decode", "tma"), ("us_prefill", "qmm")):
+                        bqd.force_kernel(kern)
+                        r[key] = round(time_call(sweep, c, sweep.weights[(proj, gs)], x, y, reps), 2)
+                    bqd.force_kernel(None)
+                    r["gbs"] = round(call_bytes(fmt, sym, M, N, K, gs) / (r["us"] * 1e-6) / 1e9, 1)
+                    rows.append(r)
+                    del x, y
+    finally:
+        bqd.set_option(bqd.OPT_KERNEL, old)
+    return rows
+
+
 QMM_CASES = [(M, N, K) for M in (32, 512, 2048) for (N, K) in [(17408, 5120), (5120, 17408)]]
 
 
@@ -796,7 +834,7 @@ def main():
     value = whole_job_gbs(sweep.bytes_per_step, args.steps, world, ms)
     value_e2e = whole_job_gbs(sweep.bytes_per_step, args.steps, world, ms_e2e)
 
-    table = configs = None
+    table = configs = mid_m = None
     if rank == 0 and not args.no_table:
         table = per_call_table(sweep, sweep.calls, sweep.weights)
         if args.table:
@@ -806,6 +844,7 @@ def main():
                     f.write(f"{r['proj']},{r['variant']},{r['gs']},{r['M']},{r['us']},{r['gbs']}\n")
         if not args.quick:
             configs = config_tables(sweep, table)
+            mid_m = mid_m_table(sweep)
 
     if rank == 0:
         peaks, src = load_peaks()
@@ -845,6 +884,12 @@ def main():
             line["per_projection"] = aggregate(table, lambda r: r["proj"])
         if configs is not None:
             line["configs"] = configs
+        if mid_m is not None:
+            line["mid_m"] = {"columns": ["proj", "variant", "gs", "M", "us", "us_decode", "us_prefill", "gbs"],
+                             "rows": [[r["proj"], r["variant"], r["gs"], r["M"], r["us"], r["us_decode"],
+                                       r["us_prefill"], r["gbs"]] for r in mid_m],
+                             "note": "us: as dispatched; us_decode: decode kernel forced (passes of 8 x rows "
+                                     "in one launch); us_prefill: prefill product forced"}
         if not args.no_qmm:
             tf_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
             for key, fmt, label in (("qmm", T5, "t5"), ("qmm_affine2", F2, "2-bit affine"),

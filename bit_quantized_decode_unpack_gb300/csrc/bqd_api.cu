@@ -131,10 +131,14 @@ static int qmv_common(const void *x, const void *w, const void *scales, const vo
         // prefill: fused unpack + tcgen05 matrix product.  Below these sizes the
         // decode kernels (all passes of their x rows in one launch) are faster
         // (measured on a 27B-class layer): the product's 128-row tiles need a
-        // wide N (gate/up: 136 tiles; down: 40) to fill the GPU at small M,
-        // and the t5 decode kernel takes 5 rows per pass against 8 for 1/2-bit
+        // wide N (gate/up: 136 tiles; down: 40) to fill the GPU at small M.
+        // t5 (8 rows per decode pass): wide layers from M = 17 (gate gs128:
+        // 36.3 us against 29.0 for two passes at M = 9..16; three passes
+        // cost more), the long-K down projection from M = 25 (24 rows: 66.5
+        // against 63.1; 32 rows: 66.6 against 85.3), narrower layers from
+        // M = 33 (5120 x 5120 at 32 rows: 37.4 against 30.8)
         const bool wide = N >= 8192;
-        const bool prefill = format == BQD_FMT_T5 ? (wide ? M > 10 : M > 15)
+        const bool prefill = format == BQD_FMT_T5 ? (wide ? M > 16 : (K >= 8192 ? M > 24 : M > 32))
                                                   : (wide ? M > (format == BQD_FMT_AFFINE2 ? 16 : 32) : M > 64);
         if ((prefill && force != 3) || force == 4) {
             int st = launch_qmm(a, s);

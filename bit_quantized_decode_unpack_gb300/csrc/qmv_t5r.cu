@@ -1,32 +1,55 @@
 // Tensor-core decode QMV for t5 ternary weights fed by TMA into a shared-memory
-// ring (M <= 5 activation rows per pass, K a multiple of 1024).
+// ring (M <= 8 activation rows per pass, K a multiple of 1024).
 //
 // Page: "oMLX Bonsai 自定义内核:Qwen 系列快速 QMV 路径完整解析" -- §二.3 (t5:
 // trits {0,1,2}, five per uint8, 13 bytes per 64-weight group / 26 per
 // 128-weight group), §二.2 (one read of every weight byte serves all M rows;
 // the sym variant rebuilds the bias from the scale).
 //
-// Arithmetic as in the register-streaming t5 kernel: a 256-entry shared table
-// maps a byte to its five trits as 2-bit fields (bits 0,2,4,6,8); byte i of
-// group 2b is paired with byte i of group 2b+1 (gs=64) or byte i with byte
-// i+26 (gs=128); per trit one LOP3 (mask + magic exponent) and one HFMA2
-// give fp16(s*t) for both halves; mma.sync m16n8k16 with fp32 accumulation
-// (weight rows = MMA rows, x rows = MMA columns); the bias term is an extra
-// MMA against the group sums of x split into fp16 high part and remainder.
-// A thread's slice of a row chunk is 52 bytes (4 groups of 64 / 2 of 128),
-// i.e. codes [256t, 256t+256) of the chunk.
+//   y[m,n] = sum_g s[n,g] * sum_{k in g} x[m,k] t[n,k]  +  sum_g b[n,g] Sx[m,g]
 //
-// CTA: 8 consumer warps (warp w owns weight rows n0+16w .. +15) and one
-// producer warp.  Per ring stage (one 1024-code chunk of the CTA's 128 rows)
-// the producer issues three 2-D TMA copies -- weights [128][208 B], scales
-// and biases [128][groups of the chunk] -- and, from the chunk of x (TMA into
-// a double buffer, one chunk ahead), builds the MMA B fragments and the
-// group sums.  Weights,
-// scales and biases are requested before the programmatic-dependent-launch
-// wait.  K is split over the S CTAs of a cluster; the partial sums are
-// reduce-scattered through distributed shared memory, each rank adding its
-// slice of rows in rank order (deterministic, no global scratch).  Every
-// mbarrier wait is bounded; an expiry is counted for bqd_device_status.
+// Decode without a table.  Two bytes a, b of one group go into the halves of
+// an fp16x2 as 1024 + v (one PRMT against the exponent byte 0x64).  Integer
+// division by three is one fused fp16 multiply-add: for Q = 1024 + q with
+// q <= 242, fma(Q, fp16(1/3), 682.5) rounds to exactly 1024 + floor(q/3)
+// (checked for every byte value).  So
+//     Q0 = V,  Q(d+1) = fma(Qd, 1/3, 682.5),  A_d = fma(Q(d+1), -3, Qd) = t_d - 2048
+// for d < 4, and A_4 = Q4 = 1024 + t_4: eight HFMA2 give the five digits of
+// both bytes exactly.  A group's byte without a partner pairs two of its own
+// digits: its high half starts one division ahead.
+//
+// Layout of the codes on the MMA (mma.sync m16n8k16, fp32 accumulation,
+// weight rows = MMA rows): thread t of a quad takes codes [256t, 256t+256)
+// of a row's 1024-code chunk (four whole groups of 64, or two of 128), one
+// group ("period") at a time; its k-slots of MMA i of a period hold items 2i
+// and 2i+1 of that group (item = the two codes of one A register).  Two ways
+// to apply the scale:
+//  * column split (passes of M <= 2 x rows): B column 2t+e holds x row e at
+//    thread t's k-slots and zeros at the other threads' slots, so D[n][2t+e]
+//    sums thread t's current group alone, and s (D - Cx) + b Sx adds it in
+//    fp32.  Cx (the offsets' dot product) and Sx (the group sum of x) come
+//    from the same MMA sequence over a constant A (row 0 ones, row 1 the
+//    offsets), run once per chunk by the producer: a row whose trits in a
+//    group are all zero gives D == Cx bit for bit.  No weight is scaled.
+//  * scaled (M >= 3): fma(A, s, 2048 s) (or -1024 s for digit 4) gives
+//    fp16(s t) exactly while |s| < 32 (a warp with larger scales takes the
+//    exact (A + 2048) s form), the B columns are the x rows, and one MMA per
+//    A fragment serves all M <= 8 rows.  The bias term is one MMA per two
+//    groups per chunk, against the group sums of x split into an fp16 high
+//    part and remainder.
+//
+// CTA: NW consumer warps (warp w owns weight rows n0+16w .. +15) and one
+// producer warp; NW = 8 (128 rows, two CTAs per SM) for passes of up to five
+// x rows, 16 (256 rows, one CTA per SM) for larger passes.  Per ring stage (one 1024-code chunk of
+// the CTA's rows) the producer issues the 2-D TMA copies of the weights
+// [rows][208 B], the scales and the biases, then builds the B fragments from
+// the chunk of x (TMA into a double buffer, one chunk ahead; each pass of the
+// warp gathers from one x row) and the sums above.  Weights, scales and
+// biases are requested before the programmatic-dependent-launch wait.  K is
+// split over the S CTAs of a cluster.  The partial sums are reduce-scattered
+// through distributed shared memory, each rank adding its slice of rows in
+// rank order (deterministic, no global scratch).  Every mbarrier wait is
+// bounded.  An expiry is counted for bqd_device_status.
 #include <cudaTypedefs.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -45,19 +68,27 @@ using namespace qmvdev;
 
 __device__ unsigned int g_qmv_t5r_timeouts = 0;
 
-constexpr int kConsR = 8;                      // consumer warps
-constexpr int kThreadsR = (kConsR + 1) * 32;   // + one producer warp
-constexpr int kRowsR = 16 * kConsR;            // weight rows per CTA
 constexpr int kCodesR = 1024;                  // codes per row per stage
 constexpr int kBytesR = 208;                   // t5 bytes per row per stage
-constexpr int kMmasR = 65;                     // per 16-row unit: 26 byte pairs x 5 trits x 2 / 8
-constexpr int kPairsR = 33;                    // MMA pairs (the last one half empty)
-constexpr int kMaxMR = 5;                      // x rows per pass
+constexpr int kSliceR = 52;                    // bytes of one thread's slice of a row chunk
+constexpr int kMmasR = 64;                     // MMAs per 16 rows per chunk
+constexpr int kPairsR = kMmasR / 2;            // B entries of two MMAs each, per slot and x row
+constexpr int kMaxMR = 8;                      // x rows per pass (the MMA's N)
 constexpr int kMaxStagesR = 4;
 constexpr int kMaxSplitR = 16;
-constexpr size_t kSmemBudgetR = 108 * 1024;    // two CTAs per SM, with the static tables and the 1 KB reserve
+
+// CTA shape: NW consumer warps of 16 weight rows each plus one producer warp:
+// NW = 8 (128 rows, two CTAs per SM) or NW = 16 (256 rows, one CTA per SM).
+template <int NW>
+struct Cta {
+    static constexpr int kThreads = (NW + 1) * 32;
+    static constexpr int kRows = 16 * NW;
+    static constexpr int kPerSM = NW == 16 ? 1 : 2;
+    static constexpr size_t kSmemBudget = NW == 16 ? 224 * 1024 : 110 * 1024;  // dynamic (static ~3 KB)
+};
 
 struct T5RParams {
+    const uint8_t *w;  // host side only (the weight tensor map)
     const __half *x;
     const __half *scales;
     const __half *biases;
@@ -67,41 +98,103 @@ struct T5RParams {
     int Mtot;  // x rows of the call; pass blockIdx.y takes rows M*y .. M*y+M-1
     int N, K, G, chunks, S, Cs, stages, RS;
     uint32_t stage_bytes;
-    uint32_t zero;  // always 0: keeps the magic constants opaque (in registers)
+    uint32_t zero;  // always 0: keeps the fp16 constants opaque (in registers)
     unsigned long long wait_ns;  // limit of the pipeline waits
 };
 
+// ---- the items of a group ----------------------------------------------------------
+//
+// A group of GS codes is B bytes (byte c holds codes 5c .. 5c+4, digit d = code
+// 5c + d).  It is cut into GS/2 "items", each the two halves of one A
+// register:
+//   * items 5j .. 5j+4: bytes 2j and 2j+1, digit d = item - 5j;
+//   * gs=64: items 30, 31 take byte 12 (four real codes, its digit 4 is
+//     padding) as digit pairs (0,1) and (2,3) of the byte itself;
+//   * gs=128: items 60..62 take bytes 24 and 25, digits 0..2 (digits 3, 4
+//     of byte 25 are padding); item 63 takes digits (3,4) of byte 24.
+// MMA i of a group period uses items 2i (k-slots 2t, 2t+1) and 2i+1 (slots
+// 2t+8, 2t+9).
 template <int GS>
-struct G5 {
-    static constexpr int B = GS == 64 ? 13 : 26;     // bytes per group
-    static constexpr int NG = GS == 64 ? 4 : 2;      // groups per thread slice
-    static constexpr int NB = GS == 64 ? 2 : 1;      // bias MMAs per chunk
-    static constexpr int GPC = kCodesR / GS;         // groups per chunk
-    // pair j (0..25) of a slice: byte a (group 2*beta) with byte a + B (group 2*beta+1)
-    __host__ __device__ static constexpr int beta(int j) { return j / B; }
-    __host__ __device__ static constexpr int byte_a(int j) { return 2 * B * (j / B) + j % B; }
-    // code of the chunk behind half `hi` of half2 h of slot t's slice, or -1 (padding trit)
-    __host__ __device__ static constexpr int code(int h, int hi, int t)
+struct T5G {
+    static constexpr int B = GS == 64 ? 13 : 26;   // bytes per group
+    static constexpr int NG = kCodesR / 4 / GS;    // groups per thread slice: 4 or 2
+    static constexpr int NB = NG / 2;              // bias MMAs per chunk (two groups each)
+    static constexpr int GPC = kCodesR / GS;       // groups per chunk
+    static constexpr int MPG = GS / 4;             // MMAs per group period (a thread fills 4 k-slots of each)
+    static constexpr int NP = GS == 64 ? 6 : 12;   // full byte pairs (five items each)
+    __host__ __device__ static constexpr int byte_a(int u) { return u < 5 * NP ? 2 * (u / 5) : (GS == 64 ? 12 : 24); }
+    // the partner byte of item u, or -1 when the item pairs two digits of byte_a
+    __host__ __device__ static constexpr int byte_b(int u)
     {
-        const int j = h / 5, d = h % 5;
-        const int o = byte_a(j) + hi * B;
-        const int grp = o / B, bg = o % B;
-        const int within = 5 * bg + d;
-        return within < GS ? (NG * t + grp) * GS + within : -1;
+        return u < 5 * NP ? 2 * (u / 5) + 1 : (GS == 128 && u < 63 ? 25 : -1);
+    }
+    // digit of the low half (the high half holds the same digit of byte_b, or
+    // digit + 1 of byte_a)
+    __host__ __device__ static constexpr int digit(int u)
+    {
+        return u < 5 * NP ? u % 5 : (GS == 64 ? (u == 30 ? 0 : 2) : (u < 63 ? u - 60 : 3));
+    }
+    __host__ __device__ static constexpr int code_lo(int u) { return 5 * byte_a(u) + digit(u); }
+    __host__ __device__ static constexpr int code_hi(int u)
+    {
+        return byte_b(u) >= 0 ? 5 * byte_b(u) + digit(u) : 5 * byte_a(u) + digit(u) + 1;
     }
 };
 
-// stage layout: weights [128][208] | scales [128][GPC] | biases (if any) | B fragments [33][M][4] uint4
-// | group sums [NB][M][4] uint2
-template <int GS, bool HAS_BIAS>
+// every code of a group is exactly one half of one item
+template <int GS>
+constexpr bool items_cover_group()
+{
+    bool seen[GS] = {};
+    for (int u = 0; u < GS / 2; ++u) {
+        const int lo = T5G<GS>::code_lo(u), hi = T5G<GS>::code_hi(u);
+        if (lo < 0 || lo >= GS || hi < 0 || hi >= GS || lo == hi || seen[lo] || seen[hi]) return false;
+        seen[lo] = seen[hi] = true;
+    }
+    return true;
+}
+static_assert(items_cover_group<64>() && items_cover_group<128>(), "t5 item plan must cover every code once");
+static_assert(T5G<64>::NG * T5G<64>::MPG == kMmasR && T5G<128>::NG * T5G<128>::MPG == kMmasR,
+              "a chunk is kMmasR MMAs per 16 rows");
+
+// codes (within the group) of each item half, for the B gather table
+struct T5Items {
+    uint8_t lo[2][64], hi[2][64];  // [gs == 128][item]
+};
+
+constexpr T5Items make_t5_items()
+{
+    T5Items tb{};
+    for (int u = 0; u < 32; ++u) {
+        tb.lo[0][u] = (uint8_t)T5G<64>::code_lo(u);
+        tb.hi[0][u] = (uint8_t)T5G<64>::code_hi(u);
+    }
+    for (int u = 0; u < 64; ++u) {
+        tb.lo[1][u] = (uint8_t)T5G<128>::code_lo(u);
+        tb.hi[1][u] = (uint8_t)T5G<128>::code_hi(u);
+    }
+    return tb;
+}
+
+__constant__ T5Items c_t5 = make_t5_items();
+
+// stage layout: weights [rows][208] | scales [rows][GPC] | biases (if any)
+// | B fragments [32][M][4] uint4 | then either the group sums (hi, lo)
+// [NB][M][4] uint2 of the bias MMAs, or (column split) {Sx, Cx} of x rows
+// 0, 1 per (period, slot) [NG][4] float4 and 64 zero bytes (128-aligned)
+template <int GS, bool HAS_BIAS, bool COL, int NW>
 struct Stage5 {
-    static constexpr int kW = kRowsR * kBytesR;
-    static constexpr int kS = kRowsR * G5<GS>::GPC * 2;
+    static constexpr int kW = Cta<NW>::kRows * kBytesR;
+    static constexpr int kS = Cta<NW>::kRows * T5G<GS>::GPC * 2;
     static constexpr int kScale = kW;
     static constexpr int kBias = kW + kS;
     static constexpr int kB = kW + kS * (HAS_BIAS ? 2 : 1);
     __host__ __device__ static constexpr int sx_off(int M) { return kB + kPairsR * M * 64; }
-    __host__ __device__ static constexpr int bytes(int M) { return (sx_off(M) + G5<GS>::NB * M * 32 + 127) / 128 * 128; }
+    __host__ __device__ static constexpr int zero_off(int M) { return (sx_off(M) + T5G<GS>::NG * 4 * 16 + 127) / 128 * 128; }
+    __host__ __device__ static constexpr int bytes(int M)
+    {
+        return ((COL ? zero_off(M) + 64 : sx_off(M) + T5G<GS>::NB * M * 32) + 127) / 128 * 128;
+    }
 };
 
 // pipeline waits give up after the call's limit; drain waits after a second
@@ -129,6 +222,8 @@ __device__ __forceinline__ void sts128(uint32_t a, uint4 v)
     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// loads of data written before the stage's full barrier completed (ordered by
+// the volatile wait that precedes them in program order)
 __device__ __forceinline__ uint4 lds128r(uint32_t a)
 {
     uint4 v;
@@ -136,11 +231,18 @@ __device__ __forceinline__ uint4 lds128r(uint32_t a)
     return v;
 }
 
-__device__ __forceinline__ uint32_t mad_u32(uint32_t a, uint32_t b, uint32_t c)
+__device__ __forceinline__ uint32_t lds32r(uint32_t a)
 {
-    uint32_t d;
-    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds64r(uint32_t a)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
 }
 
 __device__ __forceinline__ void mma_r(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
@@ -158,19 +260,79 @@ __device__ __forceinline__ void st_cluster_v2r(uint32_t local_addr, uint32_t ran
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(a), "f"(b) : "memory");
 }
 
-template <int GS, bool HAS_BIAS>
-__global__ void __launch_bounds__(kThreadsR, 2)
+// fp16x2 constants of the decode (in registers)
+struct T5Consts {
+    uint32_t third;  // (1/3, 1/3)
+    uint32_t c682;   // (682.5, 682.5)
+    uint32_t m3;     // (-3, -3)
+    uint32_t e64;    // 0x64006400: the exponent byte of 1024 in both halves
+};
+
+// 1024 + byte as fp16 of slice bytes oa (low half) and ob (high half)
+__device__ __forceinline__ uint32_t v_pair(const uint32_t (&w)[13], int oa, int ob, uint32_t e64)
+{
+    const int wa = oa >> 2, wb = ob >> 2;
+    if (wa == wb) return __byte_perm(w[wa], e64, (uint32_t)((oa & 3) | (5 << 4) | ((ob & 3) << 8) | (7 << 12)));
+    const uint32_t v = __byte_perm(w[wa], w[wb], (uint32_t)((oa & 3) | ((4 + (ob & 3)) << 8)));
+    return __byte_perm(v, e64, 0x7250u);
+}
+
+// The A register of item u of group period P for one row whose slice words are
+// w[13] (bytes 52t .. 52t+51 of the row's chunk), before scaling: t - 2048 in
+// each half, or t + 1024 for digit 4 of a pair.  Called in fully unrolled
+// loops: P and u fold to constants (w[] stays in registers, selectors are
+// immediates) and the divisions shared by a pair's five items merge.
+template <int GS>
+__device__ __forceinline__ uint32_t item_raw(int P, int u, const uint32_t (&w)[13], const T5Consts &k)
+{
+    using Ge = T5G<GS>;
+    const int oa = Ge::B * P + Ge::byte_a(u);
+    const int d = Ge::digit(u);
+    uint32_t q[6];
+    if (Ge::byte_b(u) >= 0) {
+        q[0] = v_pair(w, oa, Ge::B * P + Ge::byte_b(u), k.e64);
+    } else {
+        // digits d, d+1 of one byte: the high half starts one division ahead
+        // (gs=128: byte 24 is also the low byte of the pair (24, 25))
+        const uint32_t v = v_pair(w, oa, GS == 128 ? Ge::B * P + 25 : oa, k.e64);
+        q[0] = __byte_perm(v, hfma2(v, k.third, k.c682), 0x5410);
+    }
+#pragma unroll
+    for (int j = 0; j < 5; ++j)
+        if (j <= d) q[j + 1] = hfma2(q[j], k.third, k.c682);
+    return d < 4 || Ge::byte_b(u) < 0 ? hfma2(q[d + 1], k.m3, q[d]) : q[4];
+}
+
+// offset class of item u: 0 = t - 2048, 1 = t + 1024
+template <int GS>
+__host__ __device__ constexpr int item_off(int u)
+{
+    return T5G<GS>::byte_b(u) >= 0 && T5G<GS>::digit(u) == 4 ? 1 : 0;
+}
+
+// fp16(s t) from an item: fma(A, s, -off s) is exact while |s| < 32; else (A - off) s
+template <bool FAST>
+__device__ __forceinline__ uint32_t scale_item(uint32_t a, uint32_t s2, uint32_t ks2, uint32_t off2)
+{
+    return FAST ? hfma2(a, s2, ks2) : hmul2(hsub2(a, off2), s2);
+}
+
+// COL: column split (passes of M <= 2 x rows), see the file comment
+template <int GS, bool HAS_BIAS, bool COL, int NW>
+__global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
     qmv_t5r_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap,
                    const __grid_constant__ CUtensorMap bmap, const __grid_constant__ CUtensorMap xmap, const T5RParams p)
 {
-    using Ge = G5<GS>;
-    using SL = Stage5<GS, HAS_BIAS>;
-    constexpr int B = Ge::B;
+    using Ge = T5G<GS>;
+    using SL = Stage5<GS, HAS_BIAS, COL, NW>;
+    constexpr int kRowsR = Cta<NW>::kRows;
+    constexpr int kThreadsR = Cta<NW>::kThreads;
+    constexpr int NG = Ge::NG;
     constexpr int GPC = Ge::GPC;
+    constexpr int MPG = Ge::MPG;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStagesR], empty_bar[kMaxStagesR], x_bar[2];
-    __shared__ uint32_t lut[256];
-    __shared__ __align__(16) uint16_t koff[kPairsR * 4 * 8];  // (pair, slot) -> staging offsets of its 8 codes
+    __shared__ __align__(16) uint16_t koff[kPairsR * 4 * 8];  // (pair, slot, half) -> staging offset
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -186,6 +348,8 @@ __global__ void __launch_bounds__(kThreadsR, 2)
     // the next kernel may launch now: it only prefetches its weights until
     // its griddepcontrol.wait, which waits for this whole grid
     pdl_launch_dependents();
+    // split phase: every CTA of the cluster has started before any
+    // distributed-shared-memory store (the matching wait is before them)
     if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -194,39 +358,36 @@ __global__ void __launch_bounds__(kThreadsR, 2)
     const uint32_t XB = (uint32_t)(M * kCodesR * 2);
     float *red = reinterpret_cast<float *>(smem + (size_t)NST * STB + 2 * (size_t)XB);  // [S][RS][8]
 
-    // decode table: byte -> five trits at bits 0,2,4,6,8 (invalid bytes -> 0)
-    if (tid < 256) {
-        int v = tid, e = 0;
-        if (v < 243) {
-#pragma unroll
-            for (int d = 0; d < 5; ++d) {
-                e |= (v % 3) << (2 * d);
-                v /= 3;
-            }
-        }
-        lut[tid] = (uint32_t)e;
+    // B fragment column of this thread.  Plain: x row g (columns >= M read a
+    // valid row; their outputs are dropped).  Column split: column g is x
+    // row g & 1 at the k-slots of thread g >> 1, so this thread's entries
+    // exist only when g >> 1 == t; otherwise it reads the stage's zero bytes.
+    const int mcol = min(g, M - 1);
+    uint32_t bqo = (uint32_t)(SL::kB + (mcol * 4 + t) * 16);
+    uint32_t bstride = (uint32_t)(M * 64);
+    if constexpr (COL) {
+        // (the zero granule of lane pair g >> 1 avoids the banks that the active
+        // thread of its quarter-warp reads: no conflict between the two)
+        const bool act = (g >> 1) == t && (g & 1) < M;
+        bqo = act ? (uint32_t)(SL::kB + ((g & 1) * 4 + t) * 16) : (uint32_t)(SL::zero_off(M) + (((g >> 1) + 2) & 3) * 16);
+        bstride = act ? (uint32_t)(M * 64) : 0u;
     }
-    for (int e = tid; e < kPairsR * 4 * 8; e += kThreadsR) {
-        const int q = e & 7, slot = (e >> 3) & 3, ip = e >> 5;
-        const int i = 2 * ip + (q >> 2);  // MMA index
-        const int qq = q & 3, sl = qq >> 1, hi = qq & 1;
-        // staging layout [box k/256][row m][256] fp16: code k of row m sits at
-        // this offset + 512 m.  Padding trits point at code 0: their A entries
-        // are constant zeros, so only a finite x value is needed there.
-        const int kc = i < kMmasR ? Ge::code(2 * i + sl, hi, slot) : -1;
-        koff[e] = (uint16_t)(kc < 0 ? 0 : ((kc >> 8) * M * 512 + (kc & 255) * 2));
-    }
+
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(smem_addr(&full_bar[s]), 33);  // producer lane 0 (expect_tx) + 32 once x is prepared
-            mbar_init(smem_addr(&empty_bar[s]), kConsR * 32);
+            mbar_init(smem_addr(&empty_bar[s]), NW * 32);
         }
         mbar_init(smem_addr(&x_bar[0]), 1);
         mbar_init(smem_addr(&x_bar[1]), 1);
     }
+    if constexpr (COL) {
+        for (int i = tid; i < 4 * NST; i += kThreadsR)
+            sts128(ring_a + (uint32_t)(i >> 2) * STB + (uint32_t)(SL::zero_off(M) + (i & 3) * 16), make_uint4(0, 0, 0, 0));
+    }
     __syncthreads();
 
-    if (warp == kConsR) {
+    if (warp == NW) {
         // ---- producer ----------------------------------------------------------------
         auto issue = [&](int it, int s) {
             if (lane == 0) {
@@ -253,6 +414,31 @@ __global__ void __launch_bounds__(kThreadsR, 2)
         };
         const int pre = min(NST, ncl);
         for (int it = 0; it < pre; ++it) issue(it, it);
+        // B gather table: entry (pair ip, slot, q) is half q & 1 of item 2i + ((q >> 1) & 1)
+        // of MMA 2ip + (q >> 2) = period pp, MMA i; staging layout [box k/256][x row][256]
+        for (int e = lane; e < kPairsR * 4 * 8; e += 32) {
+            const int q = e & 7, slot = (e >> 3) & 3, ip = e >> 5;
+            const int i0 = 2 * ip + (q >> 2);
+            const int pp = i0 / MPG, i = i0 % MPG;
+            const int u = 2 * i + ((q >> 1) & 1);
+            const int code = (q & 1) ? c_t5.hi[GS == 128][u] : c_t5.lo[GS == 128][u];
+            const int kc = (NG * slot + pp) * GS + code;
+            koff[e] = (uint16_t)((kc >> 8) * M * 512 + (kc & 255) * 2);
+        }
+        // indicator A rows of the group sums: row r is 1 on the k-slots of
+        // group r (thread t's slots of period P hold group NG t + P)
+        uint32_t ind0[NG], ind1[NG];
+#pragma unroll
+        for (int P = 0; P < NG; ++P) {
+            ind0[P] = g == NG * t + P ? 0x3C003C00u : 0u;
+            ind1[P] = g + 8 == NG * t + P ? 0x3C003C00u : 0u;
+        }
+        // column split: A row 0 ones, row 1 the item offset (-2048, or +1024 for
+        // digit 4 of a pair) in both halves, rows 2..15 zero
+        uint32_t aofs[2];
+        aofs[0] = g == 0 ? 0x3C003C00u : (g == 1 ? (0xE800E800u ^ p.zero) : 0u);
+        aofs[1] = g == 0 ? 0x3C003C00u : (g == 1 ? (0x64006400u ^ p.zero) : 0u);
+        __syncwarp();
         pdl_wait();
         if (ncl > 0) issue_x(0);
         int s = 0, done = 0, issued_w = pre;
@@ -275,68 +461,83 @@ __global__ void __launch_bounds__(kThreadsR, 2)
             // see the __syncwarp below): order those reads before the next copy
             fence_proxy_async_smem();
             if (it + 1 < ncl) issue_x(it + 1);
-            // staging buffer: box j holds rows 0..M-1 of codes [256 j, 256 j + 256)
             const uint32_t xb = xraw_a + (uint32_t)(it & 1) * XB;
-            // B fragments: entry (pair ip, column m, slot) = two MMAs' (b0, b1)
-            for (int e = lane; e < kPairsR * 4; e += 32) {
-                const int ip = e >> 2, slot = e & 3;
-                const uint4 kw = lds128r(smem_addr(&koff[e * 8]));
-                const uint32_t o[8] = {xb + (kw.x & 0xffffu), xb + (kw.x >> 16), xb + (kw.y & 0xffffu), xb + (kw.y >> 16),
-                                       xb + (kw.z & 0xffffu), xb + (kw.z >> 16), xb + (kw.w & 0xffffu), xb + (kw.w >> 16)};
-                const uint32_t dst = st + SL::kB + (uint32_t)((ip * M * 4 + slot) * 16);
+            // B fragments: entry (ip, x row m, slot) at kB + ((ip M + m) 4 + slot) 16.
+            // Each pass of the warp gathers from one x row (rows are 512 bytes
+            // apart in the staging buffer: mixing them would stack bank conflicts)
+#pragma unroll 2
+            for (int k = 0; k < 4 * M; ++k) {
+                const int m = k >> 2, el = ((k & 3) << 5) | lane;
+                const int ip = el >> 2, slot = el & 3;
+                const int e = (ip * M + m) * 4 + slot;
+                const uint4 kw = *reinterpret_cast<const uint4 *>(&koff[(ip * 4 + slot) * 8]);
+                const uint32_t xm = xb + (uint32_t)(512 * m);
+                const uint32_t o[8] = {xm + (kw.x & 0xffffu), xm + (kw.x >> 16), xm + (kw.y & 0xffffu), xm + (kw.y >> 16),
+                                       xm + (kw.z & 0xffffu), xm + (kw.z >> 16), xm + (kw.w & 0xffffu), xm + (kw.w >> 16)};
+                uint32_t h[8];
 #pragma unroll
-                for (int m = 0; m < kMaxMR; ++m) {
-                    if (m < M) {
-                        uint32_t h[8];
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            uint16_t v16;
-                            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v16) : "r"(o[q] + (uint32_t)(512 * m)));
-                            h[q] = v16;
-                        }
-                        sts128(dst + (uint32_t)(64 * m), make_uint4(__byte_perm(h[0], h[1], 0x5410), __byte_perm(h[2], h[3], 0x5410),
-                                                                   __byte_perm(h[4], h[5], 0x5410), __byte_perm(h[6], h[7], 0x5410)));
-                    }
+                for (int q = 0; q < 8; ++q) {
+                    uint16_t v16;
+                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v16) : "r"(o[q]));
+                    h[q] = v16;
                 }
+                sts128(st + SL::kB + (uint32_t)(e * 16), make_uint4(__byte_perm(h[0], h[1], 0x5410), __byte_perm(h[2], h[3], 0x5410),
+                                                                   __byte_perm(h[4], h[5], 0x5410), __byte_perm(h[6], h[7], 0x5410)));
             }
             __syncwarp();
-            // group sums on the tensor core: A row r is the indicator of group r
-            // (zero at padding trits), B the fragments just built, so D[r][m] =
-            // Sx[r][m]; lane (g, t) holds groups g, g+8 x columns 2t, 2t+1
-            {
-                uint32_t P[2][2];
+            if constexpr (COL) {
+                // Sx (row 0) and Cx (row 1) of every (period, slot, x row): the
+                // consumers' MMA sequence (two chains per period) over a constant A
 #pragma unroll
-                for (int be = 0; be < 2; ++be)
+                for (int P = 0; P < NG; ++P) {
+                    float d2[2][4];
 #pragma unroll
-                    for (int rh = 0; rh < 2; ++rh) {
-                        const int row = g + 8 * rh, ga = Ge::NG * t + 2 * be;
-                        P[be][rh] = (ga == row ? 0x3C00u : 0u) | (ga + 1 == row ? 0x3C000000u : 0u);
+                    for (int q = 0; q < 4; ++q) d2[0][q] = d2[1][q] = 0.f;
+#pragma unroll
+                    for (int i = 0; i < MPG; i += 2) {
+                        const int ic = P * MPG + i;
+                        const uint4 bv = lds128r(st + bqo + (uint32_t)(ic >> 1) * bstride);
+                        mma_r(d2[(i >> 1) & 1], aofs[item_off<GS>(2 * i)], 0u, aofs[item_off<GS>(2 * i + 1)], 0u, bv.x, bv.y);
+                        mma_r(d2[(i >> 1) & 1], aofs[item_off<GS>(2 * i + 2)], 0u, aofs[item_off<GS>(2 * i + 3)], 0u, bv.z,
+                              bv.w);
                     }
-                float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-                const uint32_t bq = st + SL::kB + (uint32_t)((min(g, M - 1) * 4 + t) * 16);
-                uint4 bv = make_uint4(0, 0, 0, 0);
-#pragma unroll
-                for (int i = 0; i < kMmasR; ++i) {
-                    if ((i & 1) == 0) bv = lds128r(bq + (uint32_t)((i >> 1) * M * 64));
-                    const int h0 = 2 * i, h1 = 2 * i + 1;
-                    const bool pad0 = 5 * ((h0 / 5) % B) + h0 % 5 >= GS, pad1 = 5 * ((h1 / 5) % B) + h1 % 5 >= GS;
-                    const int be0 = Ge::beta(h0 / 5), be1 = Ge::beta(h1 / 5);
-                    const uint32_t a0 = pad0 ? 0u : P[be0][0], a1 = pad0 ? 0u : P[be0][1];
-                    const uint32_t a2 = pad1 ? 0u : P[be1][0], a3 = pad1 ? 0u : P[be1][1];
-                    mma_r((i & 1) ? d1 : d0, a0, a1, a2, a3, (i & 1) ? bv.z : bv.x, (i & 1) ? bv.w : bv.y);
+                    if (g < 2) {
+                        const uint32_t a = st + (uint32_t)SL::sx_off(M) + (uint32_t)((P * 4 + t) * 16 + 4 * g);
+                        // float4 {Sx(x row 0), Cx(0), Sx(1), Cx(1)}: thread g writes elements g, g + 2
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(d2[0][0] + d2[1][0]) : "memory");
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(a + 8), "f"(d2[0][1] + d2[1][1]) : "memory");
+                    }
                 }
+            } else {
+                // group sums on the tensor core: D[r][m] = Sx[group r][x row m];
+                // thread (g, t) holds groups g, g+8 of x rows 2t, 2t+1
+                {
+                    float d4[4][4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int r = g + 8 * (q >> 1), m = 2 * t + (q & 1);
-                    if (r < GPC && m < M) {
-                        const float v = d0[q] + d1[q];
-                        const __half hi = __float2half_rn(v);
-                        const __half lo = __float2half_rn(v - __half2float(hi));
-                        const int slot = r / Ge::NG, rem = r % Ge::NG, nb = rem >> 1, s_ = rem & 1;
-                        const uint32_t a = st + (uint32_t)SL::sx_off(M) + (uint32_t)(((nb * M + m) * 4 + slot) * 8 + 4 * s_);
-                        asm volatile("st.shared.u32 [%0], %1;" ::"r"(a),
-                                     "r"((uint32_t)__half_as_ushort(hi) | ((uint32_t)__half_as_ushort(lo) << 16))
-                                     : "memory");
+                    for (int q = 0; q < 4; ++q) d4[q][0] = d4[q][1] = d4[q][2] = d4[q][3] = 0.f;
+#pragma unroll
+                    for (int P = 0; P < NG; ++P)
+#pragma unroll
+                        for (int i = 0; i < MPG; i += 2) {
+                            const int ic = P * MPG + i;
+                            const uint4 bv = lds128r(st + bqo + (uint32_t)(ic >> 1) * bstride);
+                            mma_r(d4[(ic >> 1) & 3], ind0[P], ind1[P], ind0[P], ind1[P], bv.x, bv.y);
+                            mma_r(d4[(ic >> 1) & 3], ind0[P], ind1[P], ind0[P], ind1[P], bv.z, bv.w);
+                        }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int r = g + 8 * (q >> 1), m = 2 * t + (q & 1);
+                        if (r < GPC && m < M) {
+                            const float v = (d4[0][q] + d4[1][q]) + (d4[2][q] + d4[3][q]);
+                            const __half hi = __float2half_rn(v);
+                            const __half lo = __float2half_rn(v - __half2float(hi));
+                            // bias MMA nb: slots 2t, 2t+1 <- group NG t + 2nb, slots 2t+8, 2t+9 <- group NG t + 2nb + 1
+                            const int slot = r / NG, rem = r % NG, nb = rem >> 1, h2 = rem & 1;
+                            const uint32_t a = st + (uint32_t)SL::sx_off(M) + (uint32_t)(((nb * M + m) * 4 + slot) * 8 + 4 * h2);
+                            asm volatile("st.shared.u32 [%0], %1;" ::"r"(a),
+                                         "r"((uint32_t)__half_as_ushort(hi) | ((uint32_t)__half_as_ushort(lo) << 16))
+                                         : "memory");
+                        }
                     }
                 }
             }
@@ -367,124 +568,169 @@ __global__ void __launch_bounds__(kThreadsR, 2)
     }
 
     // ---- consumers -------------------------------------------------------------------
-    uint32_t mg[5];
-#pragma unroll
-    for (int d = 0; d < 5; ++d) mg[d] = magic(2 * d) ^ p.zero;
+    T5Consts kc;
+    kc.third = 0x35553555u ^ p.zero;
+    kc.c682 = 0x61556155u ^ p.zero;
+    kc.m3 = 0xC200C200u ^ p.zero;
+    kc.e64 = 0x64006400u ^ p.zero;
+    const uint32_t c2048 = 0x68006800u ^ p.zero, cm1024 = 0xE400E400u ^ p.zero;  // (2048, 2048), (-1024, -1024)
+    const uint32_t off0 = 0xE800E800u ^ p.zero, off1 = 0x64006400u ^ p.zero;    // item offsets -2048, +1024
     float acc[4][4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
-    const int mcol = min(g, M - 1);  // columns >= M read a valid column; their outputs are dropped
     const int r0 = warp * 16 + g;
     uint32_t st_a = ring_a;
     int s = 0;
     uint32_t par = 0;
     for (int it = 0; it < ncl; ++it) {
         if (!wait_bounded_r(smem_addr(&full_bar[s]), par, p.wait_ns)) break;
-        // this lane's 52-byte slices of rows r0 and r0+8
-        uint32_t wa[13], wb[13];
-#pragma unroll
-        for (int q = 0; q < 13; ++q) {
-            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wa[q]) : "r"(st_a + (uint32_t)(r0 * kBytesR + 52 * t + 4 * q)));
-            asm volatile("ld.shared.u32 %0, [%1];"
-                         : "=r"(wb[q])
-                         : "r"(st_a + (uint32_t)((r0 + 8) * kBytesR + 52 * t + 4 * q)));
-        }
-        // scales (and biases) of this slice's groups, rows r0 and r0+8
-        uint16_t sv[2][Ge::NG], bv[2][Ge::NG];
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            const uint32_t sa = st_a + SL::kScale + (uint32_t)(((r0 + 8 * rr) * GPC + Ge::NG * t) * 2);
-            uint32_t sw[2] = {0u, 0u}, bw[2] = {0u, 0u};
-            if (Ge::NG == 4) {
-                asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(sw[0]), "=r"(sw[1]) : "r"(sa));
-                if (HAS_BIAS)
-                    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(bw[0]), "=r"(bw[1]) : "r"(sa + SL::kS));
-            } else {
-                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sw[0]) : "r"(sa));
-                if (HAS_BIAS) asm volatile("ld.shared.u32 %0, [%1];" : "=r"(bw[0]) : "r"(sa + SL::kS));
-            }
-#pragma unroll
-            for (int q = 0; q < Ge::NG; ++q) {
-                sv[rr][q] = (uint16_t)(sw[q >> 1] >> (16 * (q & 1)));
-                bv[rr][q] = HAS_BIAS ? (uint16_t)(bw[q >> 1] >> (16 * (q & 1)))
-                                     : __half_as_ushort(sym_bias(__ushort_as_half(sv[rr][q]), p.ratio));
-            }
-        }
-        // per pair-block beta: s2 = (s[2b], s[2b+1]) and c_d = -2^(10-2d) * s2
-        constexpr int NBETA = GS == 64 ? 2 : 1;
-        uint32_t s2[2][NBETA], cst[2][NBETA][5];
+        // scales (and biases) of this thread's groups NG t .. NG t + NG - 1, rows r0, r0+8
+        uint32_t sw[2][NG / 2], bw[2][NG / 2];
         bool fast = true;
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-            for (int be = 0; be < NBETA; ++be) {
-                s2[rr][be] = (uint32_t)sv[rr][2 * be] | ((uint32_t)sv[rr][2 * be + 1] << 16);
-#pragma unroll
-                for (int d = 0; d < 5; ++d)
-                    cst[rr][be][d] =
-                        hmul2(s2[rr][be], dup_half(__half_as_ushort(__float2half_rn(-(float)(1024 >> (2 * d))))));
-                // the constants stay finite for |s| < 63; else the exact (magic - offset) * s form
-                fast = fast && fabsf(__half2float(__ushort_as_half(sv[rr][2 * be]))) < 63.f &&
-                       fabsf(__half2float(__ushort_as_half(sv[rr][2 * be + 1]))) < 63.f;
+        for (int rr = 0; rr < 2; ++rr) {
+            const uint32_t sa = st_a + SL::kScale + (uint32_t)(((r0 + 8 * rr) * GPC + NG * t) * 2);
+            if constexpr (NG == 4) {
+                const uint2 v = lds64r(sa);
+                sw[rr][0] = v.x;
+                sw[rr][1] = v.y;
+                if constexpr (HAS_BIAS) {
+                    const uint2 b = lds64r(sa + SL::kS);
+                    bw[rr][0] = b.x;
+                    bw[rr][1] = b.y;
+                }
+            } else {
+                sw[rr][0] = lds32r(sa);
+                if constexpr (HAS_BIAS) bw[rr][0] = lds32r(sa + SL::kS);
             }
-        const bool all_fast = __all_sync(0xffffffffu, fast);
-        const uint32_t bq = st_a + SL::kB + (uint32_t)((mcol * 4 + t) * 16);
-        const uint32_t bstride = (uint32_t)(M * 64);
-
-        auto pairs = [&](auto fast_tag) {
-            constexpr bool kFast = decltype(fast_tag)::value;
-            uint4 bcur = make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int jp = 0; jp < 13; ++jp) {
-                uint32_t A0[10], A1[10];
+            for (int q = 0; q < NG / 2; ++q) {
+                const __half2 h = *reinterpret_cast<const __half2 *>(&sw[rr][q]);
+                fast = fast && fabsf(__low2float(h)) < 32.f && fabsf(__high2float(h)) < 32.f;
+            }
+        }
+        const uint32_t bq = st_a + bqo;
+        const uint32_t wra = st_a + (uint32_t)(r0 * kBytesR + kSliceR * t);
+        if constexpr (COL) {
+            // per period: D[n][2t+e] = x row e . (t_d - 2048 or t_4 + 1024) over this
+            // thread's group NG t + P, two MMA chains; then s (D - Cx) + b Sx in fp32
+            uint32_t wa[13], wb[13];
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int j = 2 * jp + jj;
-                    const int oa = Ge::byte_a(j), ob = oa + B;
-                    const int be = Ge::beta(j);
-                    const uint32_t la0 = lut[__byte_perm(wa[oa >> 2], 0, 0x4440 | (oa & 3))];
-                    const uint32_t lb0 = lut[__byte_perm(wa[ob >> 2], 0, 0x4440 | (ob & 3))];
-                    const uint32_t la1 = lut[__byte_perm(wb[oa >> 2], 0, 0x4440 | (oa & 3))];
-                    const uint32_t lb1 = lut[__byte_perm(wb[ob >> 2], 0, 0x4440 | (ob & 3))];
-                    const uint32_t v0 = mad_u32(lb0, 65536u, la0);
-                    const uint32_t v1 = mad_u32(lb1, 65536u, la1);
+            for (int P = 0; P < NG; ++P) {
 #pragma unroll
-                    for (int d = 0; d < 5; ++d) {
-                        if (5 * (j % B) + d >= GS) {  // padding trit of a group's last byte
-                            A0[5 * jj + d] = A1[5 * jj + d] = 0u;
-                            continue;
-                        }
-                        const uint32_t mask = 0x00030003u << (2 * d);
-                        const uint32_t h0 = (v0 & mask) | mg[d];
-                        const uint32_t h1 = (v1 & mask) | mg[d];
-                        if (kFast) {
-                            A0[5 * jj + d] = hfma2(h0, s2[0][be], cst[0][be][d]);
-                            A1[5 * jj + d] = hfma2(h1, s2[1][be], cst[1][be][d]);
-                        } else {
-                            A0[5 * jj + d] = hmul2(hsub2(h0, mg[d]), s2[0][be]);
-                            A1[5 * jj + d] = hmul2(hsub2(h1, mg[d]), s2[1][be]);
-                        }
+                for (int q = 0; q < 13; ++q) {
+                    const bool need = q >= (Ge::B * P) / 4 && q <= (Ge::B * P + Ge::B - 1) / 4;
+                    const bool had = P > 0 && q <= (Ge::B * P - 1) / 4;
+                    if (need && !had) {
+                        wa[q] = lds32r(wra + (uint32_t)(4 * q));
+                        wb[q] = lds32r(wra + (uint32_t)(8 * kBytesR + 4 * q));
                     }
                 }
+                float d2[2][4];
 #pragma unroll
-                for (int q = 0; q < 5; ++q) {
-                    const int i = 5 * jp + q;
-                    if ((i & 1) == 0) bcur = lds128r(bq + (uint32_t)(i >> 1) * bstride);
-                    const uint32_t b0 = (i & 1) ? bcur.z : bcur.x, b1 = (i & 1) ? bcur.w : bcur.y;
-                    mma_r(acc[i & 3], A0[2 * q], A1[2 * q], A0[2 * q + 1], A1[2 * q + 1], b0, b1);
+                for (int q = 0; q < 4; ++q) d2[0][q] = d2[1][q] = 0.f;
+#pragma unroll
+                for (int i = 0; i < MPG; i += 2) {
+                    const uint32_t a0 = item_raw<GS>(P, 2 * i, wa, kc), a1 = item_raw<GS>(P, 2 * i, wb, kc);
+                    const uint32_t a2 = item_raw<GS>(P, 2 * i + 1, wa, kc), a3 = item_raw<GS>(P, 2 * i + 1, wb, kc);
+                    const uint32_t c0 = item_raw<GS>(P, 2 * i + 2, wa, kc), c1 = item_raw<GS>(P, 2 * i + 2, wb, kc);
+                    const uint32_t c2 = item_raw<GS>(P, 2 * i + 3, wa, kc), c3 = item_raw<GS>(P, 2 * i + 3, wb, kc);
+                    const int ic = P * MPG + i;
+                    const uint4 bv = lds128r(bq + (uint32_t)(ic >> 1) * bstride);
+                    mma_r(d2[(i >> 1) & 1], a0, a1, a2, a3, bv.x, bv.y);
+                    mma_r(d2[(i >> 1) & 1], c0, c1, c2, c3, bv.z, bv.w);
+                }
+                float sc[2], bi[2];
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const uint32_t sv = sw[rr][P >> 1];
+                    const __half sh = __ushort_as_half((uint16_t)((P & 1) ? (sv >> 16) : (sv & 0xffffu)));
+                    sc[rr] = __half2float(sh);
+                    if constexpr (HAS_BIAS) {
+                        const uint32_t bv2 = bw[rr][P >> 1];
+                        bi[rr] = __half2float(__ushort_as_half((uint16_t)((P & 1) ? (bv2 >> 16) : (bv2 & 0xffffu))));
+                    } else {
+                        bi[rr] = __half2float(sym_bias(sh, p.ratio));
+                    }
+                }
+                const uint4 v = lds128r(st_a + (uint32_t)SL::sx_off(M) + (uint32_t)((P * 4 + t) * 16));
+                const float sx[2] = {__uint_as_float(v.x), __uint_as_float(v.z)};
+                const float cx[2] = {__uint_as_float(v.y), __uint_as_float(v.w)};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int rr = q >> 1, e = q & 1;
+                    acc[0][q] = fmaf(sc[rr], (d2[0][q] + d2[1][q]) - cx[e], fmaf(bi[rr], sx[e], acc[0][q]));
                 }
             }
-        };
-        if (all_fast) pairs(std::true_type{});
-        else pairs(std::false_type{});
-        // bias term: slots 2t, 2t+1 <- group NG t + 2nb, slots 2t+8, 2t+9 <- group NG t + 2nb + 1
-        const uint32_t sq = st_a + (uint32_t)SL::sx_off(M) + (uint32_t)((mcol * 4 + t) * 8);
+        } else {
+
+            // the chunk's 64 MMAs; FAST: scaled items by one HFMA2 each
+            auto body = [&](auto fast_tag) {
+                constexpr bool kFast = decltype(fast_tag)::value;
+                uint32_t wa[13], wb[13];
 #pragma unroll
-        for (int nb = 0; nb < Ge::NB; ++nb) {
-            uint32_t bx, by;
-            asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(bx), "=r"(by) : "r"(sq + (uint32_t)(nb * M * 32)));
-            mma_r(acc[nb & 3], dup_half(bv[0][2 * nb]), dup_half(bv[1][2 * nb]), dup_half(bv[0][2 * nb + 1]),
-                  dup_half(bv[1][2 * nb + 1]), bx, by);
+                for (int P = 0; P < NG; ++P) {
+                    // words holding bytes [B P, B P + B) of the slices (the first may
+                    // have been read for the previous group)
+#pragma unroll
+                    for (int q = 0; q < 13; ++q) {
+                        const bool need = q >= (Ge::B * P) / 4 && q <= (Ge::B * P + Ge::B - 1) / 4;
+                        const bool had = P > 0 && q <= (Ge::B * P - 1) / 4;
+                        if (need && !had) {
+                            wa[q] = lds32r(wra + (uint32_t)(4 * q));
+                            wb[q] = lds32r(wra + (uint32_t)(8 * kBytesR + 4 * q));
+                        }
+                    }
+                    // this group's scale in both halves, and -off * scale for the two offsets
+                    uint32_t s2[2], k0[2], k1[2];
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        s2[rr] = __byte_perm(sw[rr][P >> 1], 0u, (P & 1) ? 0x3232u : 0x1010u);
+                        k0[rr] = hmul2(s2[rr], c2048);
+                        k1[rr] = hmul2(s2[rr], cm1024);
+                    }
+#pragma unroll
+                    for (int i = 0; i < MPG; i += 2) {
+                        uint32_t A[2][4];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh) {
+                                const int u = 2 * (i + h) + hh;
+                                const bool o1 = item_off<GS>(u) == 1;
+                                A[h][2 * hh] = scale_item<kFast>(item_raw<GS>(P, u, wa, kc), s2[0], o1 ? k1[0] : k0[0],
+                                                                 o1 ? off1 : off0);
+                                A[h][2 * hh + 1] = scale_item<kFast>(item_raw<GS>(P, u, wb, kc), s2[1], o1 ? k1[1] : k0[1],
+                                                                     o1 ? off1 : off0);
+                            }
+                        const int ic = P * MPG + i;
+                        const uint4 bv = lds128r(bq + (uint32_t)(ic >> 1) * bstride);
+                        mma_r(acc[(ic >> 1) & 3], A[0][0], A[0][1], A[0][2], A[0][3], bv.x, bv.y);
+                        mma_r(acc[(ic >> 1) & 3], A[1][0], A[1][1], A[1][2], A[1][3], bv.z, bv.w);
+                    }
+                }
+            };
+            if (__all_sync(0xffffffffu, fast)) body(std::true_type{});
+            else body(std::false_type{});
+
+            // bias term: slots 2t, 2t+1 <- group NG t + 2nb, slots 2t+8, 2t+9 <- group NG t + 2nb + 1
+            const uint32_t sq = st_a + (uint32_t)SL::sx_off(M) + (uint32_t)((mcol * 4 + t) * 8);
+#pragma unroll
+            for (int nb = 0; nb < Ge::NB; ++nb) {
+                uint32_t bb[2][2];
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const uint32_t bsrc = HAS_BIAS ? bw[rr][nb] : sw[rr][nb];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint16_t v16 = (uint16_t)(bsrc >> (16 * h));
+                        bb[rr][h] = HAS_BIAS ? dup_half(v16)
+                                             : dup_half(__half_as_ushort(sym_bias(__ushort_as_half(v16), p.ratio)));
+                    }
+                }
+                const uint2 bxy = lds64r(sq + (uint32_t)(nb * M * 32));
+                mma_r(acc[nb & 3], bb[0][0], bb[1][0], bb[0][1], bb[1][1], bxy.x, bxy.y);
+            }
         }
         mbar_arrive_r(smem_addr(&empty_bar[s]));
         st_a += STB;
@@ -497,32 +743,56 @@ __global__ void __launch_bounds__(kThreadsR, 2)
     float v[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) v[q] = (acc[0][q] + acc[1][q]) + (acc[2][q] + acc[3][q]);
+    // column split: the four threads of a quad hold four groups of the same
+    // rows and x rows; add them (fixed order), then thread t writes row
+    // r0 + 8 (t >> 1), x row t & 1
+    const int rr_t = t >> 1, e_t = t & 1;
+    float vcol = 0.f;
+    if constexpr (COL) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[q] += __shfl_xor_sync(0xffffffffu, v[q], 1);
+            v[q] += __shfl_xor_sync(0xffffffffu, v[q], 2);
+        }
+        vcol = rr_t ? (e_t ? v[3] : v[2]) : (e_t ? v[1] : v[0]);
+    }
 
-    // ---- results: value q is row r0 + 8 (q >> 1), column 2t + (q & 1) -------------------
+    // ---- results: value q is row r0 + 8 (q >> 1), x row 2t + (q & 1) -------------------
     const int Mv = min(M, p.Mtot - M * (int)blockIdx.y);  // rows of this pass that exist
     __half *outg = p.out + (size_t)(M * blockIdx.y) * p.N;
     if (S == 1) {
+        if constexpr (COL) {
+            const int n = n0 + r0 + 8 * rr_t;
+            if (n < p.N && e_t < Mv) outg[(size_t)e_t * p.N + n] = __float2half_rn(vcol);
+        } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int n = n0 + r0 + 8 * (q >> 1), m = 2 * t + (q & 1);
-            if (n < p.N && m < Mv) outg[(size_t)m * p.N + n] = __float2half_rn(v[q]);
+            for (int q = 0; q < 4; ++q) {
+                const int n = n0 + r0 + 8 * (q >> 1), m = 2 * t + (q & 1);
+                if (n < p.N && m < Mv) outg[(size_t)m * p.N + n] = __float2half_rn(v[q]);
+            }
         }
         return;
     }
     const int RS = p.RS;
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int row = r0 + 8 * h;
+    if constexpr (COL) {
+        const int row = r0 + 8 * rr_t;
         const int q = row / RS;
-        st_cluster_v2r(smem_addr(red + ((size_t)rank * RS + (row - q * RS)) * 8 + 2 * t), (uint32_t)q, v[2 * h],
-                       v[2 * h + 1]);
+        if (e_t < M) st_cluster_f32(smem_addr(red + ((size_t)rank * RS + (row - q * RS)) * 8 + e_t), (uint32_t)q, vcol);
+    } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = r0 + 8 * h;
+            const int q = row / RS;
+            st_cluster_v2r(smem_addr(red + ((size_t)rank * RS + (row - q * RS)) * 8 + 2 * t), (uint32_t)q, v[2 * h],
+                           v[2 * h + 1]);
+        }
     }
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
     const int row0 = rank * RS;
     const int nrow = min(RS, kRowsR - row0);
-    for (int e = tid; e < nrow * M; e += kConsR * 32) {
-        const int lr = e / M, m = e % M;
+    for (int i = tid; i < nrow * M; i += NW * 32) {
+        const int lr = i / M, m = i % M;
         float sum = 0.f;
         for (int k = 0; k < S; ++k) sum += red[((size_t)k * RS + lr) * 8 + m];
         const int n = n0 + row0 + lr;
@@ -548,7 +818,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_r()
 }
 
 bool encode_2d(CUtensorMap &map, CUtensorMapDataType dt, const void *base, int64_t cols, int64_t rows,
-               int64_t row_bytes, int box_cols, int box_rows = kRowsR)
+               int64_t row_bytes, int box_cols, int box_rows)
 {
     auto enc = encode_fn_r();
     if (!enc) return false;
@@ -566,13 +836,13 @@ struct RPlan {
     size_t smem;
 };
 
-template <int GS, bool HAS_BIAS>
+template <int GS, bool HAS_BIAS, bool COL, int NW>
 size_t t5r_smem(int M, int S, int stages, int RS)
 {
-    return 1024 + (size_t)stages * Stage5<GS, HAS_BIAS>::bytes(M) + 2 * (size_t)M * kCodesR * 2 + (size_t)S * RS * 8 * 4;
+    return 1024 + (size_t)stages * Stage5<GS, HAS_BIAS, COL, NW>::bytes(M) + 2 * (size_t)M * kCodesR * 2 + (size_t)S * RS * 8 * 4;
 }
 
-template <int GS, bool HAS_BIAS>
+template <int GS, bool HAS_BIAS, bool COL, int NW>
 int cluster_slots_r(int S, size_t smem)
 {
     struct Entry { int dev, S; size_t smem; int slots; };
@@ -584,12 +854,12 @@ int cluster_slots_r(int S, size_t smem)
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < n; ++i)
         if (cache[i].dev == dev && cache[i].S == S && cache[i].smem == smem) return cache[i].slots;
-    auto kern = qmv_t5r_kernel<GS, HAS_BIAS>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudgetR);
+    auto kern = qmv_t5r_kernel<GS, HAS_BIAS, COL, NW>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cta<NW>::kSmemBudget);
     cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S * 64);
-    cfg.blockDim = dim3(kThreadsR);
+    cfg.blockDim = dim3(Cta<NW>::kThreads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -608,26 +878,28 @@ int cluster_slots_r(int S, size_t smem)
 }
 
 // P passes of x rows run side by side in one launch (grid rows)
-template <int GS, bool HAS_BIAS>
+template <int GS, bool HAS_BIAS, bool COL, int NW>
 bool plan_r(int M, int N, int chunks, int P, RPlan &best)
 {
+    constexpr int kRowsR = Cta<NW>::kRows;
+    constexpr size_t kSmemBudgetR = Cta<NW>::kSmemBudget;
     const int R = (N + kRowsR - 1) / kRowsR;
     const int sms = sm_count();
-    const size_t stage = Stage5<GS, HAS_BIAS>::bytes(M);
+    const size_t stage = Stage5<GS, HAS_BIAS, COL, NW>::bytes(M);
     double best_cost = 1e30;
     bool found = false;
     for (int S = 1; S <= kMaxSplitR && S <= chunks; ++S) {
         const int Cs = (chunks + S - 1) / S;
         if ((S - 1) * Cs >= chunks) continue;
         const int RS = (kRowsR + S - 1) / S;
-        const size_t fixed = t5r_smem<GS, HAS_BIAS>(M, S, 0, RS);
+        const size_t fixed = t5r_smem<GS, HAS_BIAS, COL, NW>(M, S, 0, RS);
         if (fixed + stage > kSmemBudgetR) continue;
         int st = (int)((kSmemBudgetR - fixed) / stage);
         st = std::min(st, kMaxStagesR);
         st = std::min(st, Cs);
         if (st < 1) continue;
-        const size_t sm = t5r_smem<GS, HAS_BIAS>(M, S, st, RS);
-        const int slots = S == 1 ? 2 * sms : cluster_slots_r<GS, HAS_BIAS>(S, sm);
+        const size_t sm = t5r_smem<GS, HAS_BIAS, COL, NW>(M, S, st, RS);
+        const int slots = S == 1 ? Cta<NW>::kPerSM * sms : cluster_slots_r<GS, HAS_BIAS, COL, NW>(S, sm);
         if (slots <= 0) continue;
         const int waves = (R * P + slots - 1) / slots;
         // time ~ waves x (chunks per CTA + first-stage latency and reduction,
@@ -644,44 +916,48 @@ bool plan_r(int M, int N, int chunks, int P, RPlan &best)
     return found;
 }
 
-template <int GS, bool HAS_BIAS>
-int launch_r(const T5RParams &p0, const CUtensorMap &wmap, cudaStream_t s)
+template <int GS, bool HAS_BIAS, bool COL, int NW>
+int launch_r(const T5RParams &p0, int64_t row_bytes, cudaStream_t s)
 {
+    CUtensorMap wmap;
+    if (!encode_2d(wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, p0.w, row_bytes, p0.N, row_bytes, kBytesR, Cta<NW>::kRows))
+        return BQD_ERR_UNSUPPORTED;
     RPlan pl;
     const int P = (p0.Mtot + p0.M - 1) / p0.M;
-    if (!plan_r<GS, HAS_BIAS>(p0.M, p0.N, p0.chunks, P, pl)) return BQD_ERR_UNSUPPORTED;
+    if (!plan_r<GS, HAS_BIAS, COL, NW>(p0.M, p0.N, p0.chunks, P, pl)) return BQD_ERR_UNSUPPORTED;
     T5RParams p = p0;
     p.S = pl.S;
     p.Cs = pl.Cs;
     p.stages = pl.stages;
     p.RS = pl.RS;
-    p.stage_bytes = (uint32_t)Stage5<GS, HAS_BIAS>::bytes(p.M);
-    constexpr int GPC = G5<GS>::GPC;
+    p.stage_bytes = (uint32_t)Stage5<GS, HAS_BIAS, COL, NW>::bytes(p.M);
+    constexpr int GPC = T5G<GS>::GPC;
     CUtensorMap smap, bmap;
-    if (!encode_2d(smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.scales, p.G, p.N, (int64_t)p.G * 2, GPC)) return BQD_ERR_CUDA;
+    if (!encode_2d(smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.scales, p.G, p.N, (int64_t)p.G * 2, GPC, Cta<NW>::kRows))
+        return BQD_ERR_CUDA;
     bmap = smap;
-    if (HAS_BIAS && !encode_2d(bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.biases, p.G, p.N, (int64_t)p.G * 2, GPC))
+    if (HAS_BIAS && !encode_2d(bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.biases, p.G, p.N, (int64_t)p.G * 2, GPC, Cta<NW>::kRows))
         return BQD_ERR_CUDA;
     // x: [Mtot][K] fp16, box {256 codes, M rows}; a pass's rows past Mtot read as zeros
     CUtensorMap xmap;
     if (!encode_2d(xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.x, p.K, p.Mtot, (int64_t)p.K * 2, 256, p.M))
         return BQD_ERR_CUDA;
     if (opt_debug_plan())
-        fprintf(stderr, "bqd t5r plan: N=%d K=%d M=%d (%d per pass) gs=%d -> S=%d Cs=%d stages=%d R=%d grid=%dx%d smem=%zu\n",
-                p.N, p.K, p.Mtot, p.M, GS, pl.S, pl.Cs, pl.stages, pl.R, pl.R * pl.S, P, pl.smem);
-    auto kern = qmv_t5r_kernel<GS, HAS_BIAS>;
+        fprintf(stderr, "bqd t5r plan: N=%d K=%d M=%d (%d per pass) gs=%d col=%d rows=%d -> S=%d Cs=%d stages=%d R=%d grid=%dx%d smem=%zu\n",
+                p.N, p.K, p.Mtot, p.M, GS, (int)COL, Cta<NW>::kRows, pl.S, pl.Cs, pl.stages, pl.R, pl.R * pl.S, P, pl.smem);
+    auto kern = qmv_t5r_kernel<GS, HAS_BIAS, COL, NW>;
     static int configured_dev[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured_dev[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudgetR) != cudaSuccess ||
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cta<NW>::kSmemBudget) != cudaSuccess ||
             cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
             return BQD_ERR_CUDA;
         configured_dev[dev] = 1;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.R * pl.S, P);
-    cfg.blockDim = dim3(kThreadsR);
+    cfg.blockDim = dim3(Cta<NW>::kThreads);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -722,10 +998,8 @@ int launch_qmv_t5r(const QmvArgs &a, cudaStream_t s)
         (reinterpret_cast<uintptr_t>(a.scales) & 15) || (a.biases && (reinterpret_cast<uintptr_t>(a.biases) & 15)))
         return BQD_ERR_UNSUPPORTED;
     if (a.K > (int64_t)1 << 28 || a.N > (int64_t)1 << 28) return BQD_ERR_UNSUPPORTED;
-    CUtensorMap wmap;
-    if (!encode_2d(wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w, a.row_bytes, a.N, a.row_bytes, kBytesR))
-        return BQD_ERR_UNSUPPORTED;
     T5RParams p;
+    p.w = static_cast<const uint8_t *>(a.w);
     p.scales = a.scales; p.biases = a.biases; p.ratio = a.ratio;
     p.N = (int)a.N; p.K = (int)a.K; p.G = (int)a.G;
     p.chunks = (int)(a.K / kCodesR);
@@ -742,8 +1016,23 @@ int launch_qmv_t5r(const QmvArgs &a, cudaStream_t s)
     p.Mtot = (int)a.M;
     p.x = a.x;
     p.out = a.out;
-    if (a.gs == 64) return hb ? launch_r<64, true>(p, wmap, s) : launch_r<64, false>(p, wmap, s);
-    return hb ? launch_r<128, true>(p, wmap, s) : launch_r<128, false>(p, wmap, s);
+    // passes of at most two x rows take the column split (no per-weight
+    // scaling).  Passes of up to five rows run 128-row CTAs, two per SM: a CTA
+    // that finishes frees room for the next kernel's first weight copies
+    // (programmatic dependent launch), which a 256-row CTA holding most of the
+    // SM's shared memory would block.  Passes of six or more rows need the
+    // larger B-fragment and x buffers of one 256-row CTA per SM.
+    const bool col = p.M <= 2;
+    const bool narrow = p.M <= 5;
+    const int64_t rb = a.row_bytes;
+#define BQD_T5R_LAUNCH(GSV, HBV)                                                                                 \
+    (col ? (narrow ? launch_r<GSV, HBV, true, 8>(p, rb, s) : launch_r<GSV, HBV, true, 16>(p, rb, s))           \
+         : (narrow ? launch_r<GSV, HBV, false, 8>(p, rb, s) : launch_r<GSV, HBV, false, 16>(p, rb, s)))
+    int rc;
+    if (a.gs == 64) rc = hb ? BQD_T5R_LAUNCH(64, true) : BQD_T5R_LAUNCH(64, false);
+    else rc = hb ? BQD_T5R_LAUNCH(128, true) : BQD_T5R_LAUNCH(128, false);
+#undef BQD_T5R_LAUNCH
+    return rc;
 }
 
 }  // namespace bqd
