@@ -565,9 +565,9 @@ def time_spec_verify(dev, reps: int = 20):
 
 
 def kernel_traffic_from_profiles():
-    """DRAM-bytes / algorithmic-bytes ratio of the QMV kernels over the eight
-    calls of one sweep group, captured without cache flushes between them
-    (profiles/qmv_traffic.json), or None when a kernel source changed since."""
+    """(DRAM read + write, DRAM read) / algorithmic bytes of the QMV kernels over
+    the eight calls of one sweep group, captured without cache flushes between
+    them (profiles/qmv_traffic.json), or None when a kernel source changed since."""
     p = ROOT / "profiles" / "qmv_traffic.json"
     if not p.exists():
         return None
@@ -576,7 +576,7 @@ def kernel_traffic_from_profiles():
         for src, digest in d["kernel_sha256"].items():
             if hashlib.sha256((ROOT / src).read_bytes()).hexdigest() != digest:
                 return None
-        return float(d["aggregate"])
+        return float(d["aggregate"]), float(d["aggregate_read"])
     except Exception:
         return None
 
@@ -862,10 +862,12 @@ def main():
                        "accumulate": "fp32", "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_source": src,
-                         "traffic": None if tr is None else tr * sweep.bytes_per_step,
-                         "traffic_basis": "DRAM bytes / algorithmic bytes over the eight calls of one sweep "
-                                          "group, no cache flush between them (profiles/qmv_traffic.json), "
-                                          "x bytes per step",
+                         "traffic": None if tr is None else tr[0] * sweep.bytes_per_step,
+                         "traffic_read": None if tr is None else tr[1] * sweep.bytes_per_step,
+                         "traffic_basis": "DRAM read + write (traffic) and read (traffic_read) / algorithmic "
+                                          "bytes over the eight calls of one sweep group, no cache flush between "
+                                          "them (profiles/qmv_traffic.json), x bytes per step; the writes are "
+                                          "write-backs of lines dirtied before the launches",
                          "kernel": "qmv (all 280 launches of a step)",
                          "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS},
             "e2e": {"value": value_e2e, "unit": UNIT, "h2d_bytes_per_step": sweep.h2d,
