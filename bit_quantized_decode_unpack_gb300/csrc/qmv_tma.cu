@@ -21,13 +21,14 @@
 // bias term is one m16n8k8 per chunk against the group sums Sx split into an
 // fp16 high part and remainder.
 //
-// CTA: 8 consumer warps (warp w owns weight rows n0+16w .. n0+16w+15 for the
-// CTA's whole K range) and one producer warp.  The producer streams the
-// CTA's 128 rows chunk by chunk (256 codes per row) into a ring of stages:
-// the weight tile with one 2-D TMA copy (64- or 32-byte swizzle, so the
-// quads' 32-bit reads hit 32 distinct banks), the tile's scales and biases
-// with cp.async, all completing on the stage's mbarrier.  Weights, scales
-// and biases are requested before the programmatic-dependent-launch wait.
+// CTA: 8 consumer warps (warp w owns weight rows n0+32w .. n0+32w+31 for the
+// CTA's whole K range) and two producer warps, which prepare alternate ring
+// stages (one warp alone bounded the pipeline with 8-column fragments).  The
+// producers stream the CTA's 256 rows chunk by chunk (256 codes per row) into
+// the ring: the weight tile with one 2-D TMA copy (64- or 32-byte swizzle, so
+// the quads' 32-bit reads hit 32 distinct banks), the tile's scales and
+// biases once per CTA, all completing on mbarriers.  Weights, scales and
+// biases are requested before the programmatic-dependent-launch wait.
 // K is split over the S CTAs of a thread-block cluster; the partial sums are
 // added in a fixed order through distributed shared memory into rank 0: no
 // global scratch, no atomics, bit-reproducible.  Every mbarrier wait is
@@ -52,7 +53,8 @@ using namespace qmvdev;
 __device__ unsigned int g_qmv_tma_timeouts = 0;
 
 constexpr int kCons = 8;                     // consumer warps
-constexpr int kThreadsT = (kCons + 1) * 32;  // + one producer warp
+constexpr int kProd = 2;                     // producer warps: they take alternate stages
+constexpr int kThreadsT = (kCons + kProd) * 32;
 constexpr int kChunkT = 256;                 // codes per row per stage
 constexpr int kMaxStagesT = 8;
 constexpr int kMaxSplitT = 16;  // cluster sizes above 8 are the non-portable ones
@@ -160,6 +162,10 @@ constexpr int kRowsC = kRowsW * kCons;   // weight rows per CTA
 //   | Cx [4][8] f32 | Sx as fp16 (hi, lo) [8][4]
 // The scales and biases of the CTA's whole K range sit outside the ring, one
 // TMA box each: [256 rows][BX groups] fp16.
+// a producer's staging of one chunk of x: MP rows of 256 fp16
+template <int MP>
+constexpr int kXRawBytes = MP * kChunkT * 2;
+
 template <int FMT, int GS, bool HAS_BIAS, int MP>
 struct Stage {
     static constexpr int kGPC = kChunkT / GS;
@@ -170,7 +176,6 @@ struct Stage {
     static constexpr int kBytes = (kSx + 8 * 4 * 4 + 511) / 512 * 512;  // keeps the weight tile 512-aligned
 };
 
-constexpr int kXRawBytes = 8 * kChunkT * 2;  // producer's staging of one chunk of x (8 rows)
 
 template <int FMT, int GS, bool HAS_BIAS, int MP>
 __global__ void __launch_bounds__(kThreadsT, 2)
@@ -185,6 +190,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     constexpr uint32_t CB = F::kChunkBytes;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStagesT], empty_bar[kMaxStagesT], sc_bar;
+    __shared__ int last_it[kMaxStagesT];  // iteration whose weights a stage received last (-1: none)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -193,6 +199,10 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     const int n0 = (blockIdx.x / S) * kRowsC;
     // pass blockIdx.y takes x rows 8y .. 8y+7 (M > 8 runs every pass in this one launch)
     const int M = min(8, p.M - 8 * (int)blockIdx.y);
+    // B-fragment column read by thread (g, t): with 4-column fragments
+    // columns 4..7 repeat 0..3; with 8 columns, columns past M repeat M - 1,
+    // so the producer builds only the M real rows (outputs past M are dropped)
+    const int bcol = MP == 4 ? (g & 3) : min(g, M - 1);
     const __half *xg = p.x + (size_t)(8 * blockIdx.y) * p.K;
     __half *outg = p.out + (size_t)(8 * blockIdx.y) * p.N;
     const int c_lo = rank * p.Cs;
@@ -209,10 +219,10 @@ __global__ void __launch_bounds__(kThreadsT, 2)
 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t ring_a = smem_addr(smem);
-    const uint32_t xraw_a = ring_a + (uint32_t)NST * SL::kBytes;  // [8][256] fp16
-    const uint32_t sc_a = xraw_a + kXRawBytes;                      // scales [256][BX] fp16
+    const uint32_t xraw_a = ring_a + (uint32_t)NST * SL::kBytes;  // per producer [MP][256] fp16
+    const uint32_t sc_a = xraw_a + kProd * kXRawBytes<MP>;          // scales [256][BX] fp16
     const uint32_t bi_a = sc_a + (uint32_t)(kRowsC * p.BX * 2);     // biases [256][BX] fp16
-    float *red = reinterpret_cast<float *>(smem + (size_t)NST * SL::kBytes + kXRawBytes +
+    float *red = reinterpret_cast<float *>(smem + (size_t)NST * SL::kBytes + kProd * kXRawBytes<MP> +
                                            (size_t)kRowsC * p.BX * 2 * (HAS_BIAS ? 2 : 1));  // [S][RS][8]
     // the scale box starts at a 16-byte aligned group index
     const int g0 = c_lo * GPC, gx = g0 & ~7;
@@ -225,23 +235,28 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         }
         mbar_init(smem_addr(&sc_bar), 1);
     }
+    if (tid < kMaxStagesT) last_it[tid] = -1;
     __syncthreads();
     uint32_t mg[10];
 #pragma unroll
     for (int i = 0; i < 10; ++i) mg[i] = F::magic_at(i < F::kNumMagic ? i : 0) ^ p.zero;
 
-    if (warp == kCons) {
-        // ---- producer ------------------------------------------------------------
-        // per stage: weights by TMA, scales/biases by cp.async, then x of the
-        // chunk turned into MMA B fragments, and Cx / Sx of its groups by the
-        // same MMA sequence as the consumers (row 0: all-zero codes, which
-        // unpack to exactly the magic values; row 1: ones).  With M <= 4,
-        // columns 4..7 of those MMAs carry a second group.
+    if (warp >= kCons) {
+        // ---- producers -----------------------------------------------------------
+        // Producer pw prepares the stages of chunks pw, pw + 2, ...: weights by
+        // TMA, then x of the chunk turned into MMA B fragments, and Cx / Sx of
+        // its groups by the same MMA sequence as the consumers (row 0: all-zero
+        // codes, which unpack to exactly the magic values; row 1: ones).  With
+        // M <= 4, columns 4..7 of those MMAs carry a second group.  Producer 0
+        // also loads the scale (and bias) boxes.
+        const int pw = warp - kCons;
+        const uint32_t xr_a = xraw_a + (uint32_t)(pw * kXRawBytes<MP>);
         auto issue_weights = [&](int it, int s) {
             if (lane == 0) {
                 const uint32_t bar = smem_addr(&full_bar[s]);
                 mbar_arrive_expect_tx(bar, (uint32_t)SL::kW);
                 tma_load_2d(ring_a + (uint32_t)s * SL::kBytes, &wmap, (c_lo + it) * (int)CB, n0, bar);
+                last_it[s] = it;
             }
         };
         auto load_x = [&](int it, uint4 (&xv)[MP]) {
@@ -256,20 +271,20 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         const uint32_t one2 = 0x3C003C00u;
         // scales, biases and the weights of the first stages do not depend on
         // the previous kernel
-        if (lane == 0 && ncl > 0) {
+        if (pw == 0 && lane == 0 && ncl > 0) {
             const uint32_t bx_bytes = (uint32_t)(kRowsC * p.BX * 2);
             mbar_arrive_expect_tx(smem_addr(&sc_bar), bx_bytes * (HAS_BIAS ? 2 : 1));
             tma_load_2d(sc_a, &smap, gx, n0, smem_addr(&sc_bar));
             if (HAS_BIAS) tma_load_2d(bi_a, &bmap, gx, n0, smem_addr(&sc_bar));
         }
         const int pre = min(NST, ncl);
-        for (int it = 0; it < pre; ++it) issue_weights(it, it);
+        for (int it = pw; it < pre; it += kProd) issue_weights(it, it);
         pdl_wait();
         uint4 xv[MP];
-        if (ncl > 0) load_x(0, xv);
-        int s = 0, done = 0;
-        uint32_t par = 0;
-        for (int it = 0; it < ncl; ++it) {
+        if (pw < ncl) load_x(pw, xv);
+        for (int it = pw; it < ncl; it += kProd) {
+            const int s = it % NST;
+            const uint32_t par = (uint32_t)(it / NST) & 1u;
             const uint32_t st = ring_a + (uint32_t)s * SL::kBytes;
             if (it >= NST) {
                 bool ok = lane == 0 ? wait_bounded(smem_addr(&empty_bar[s]), par ^ 1u, p.wait_ns) : true;
@@ -277,23 +292,26 @@ __global__ void __launch_bounds__(kThreadsT, 2)
                 if (!ok) break;
                 issue_weights(it, s);
             }
-            // x of this chunk -> staging rows (zeros past M), then the next chunk's loads
+            // x of this chunk -> staging rows (zeros past M with 4-column fragments;
+            // with 8 the rows past M are never read), then the next chunk's loads
 #pragma unroll
             for (int m = 0; m < MP; ++m)
-                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(xraw_a + (uint32_t)(m * 512 + 16 * lane)),
+                if (MP == 4 || m < M)
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(xr_a + (uint32_t)(m * 512 + 16 * lane)),
                              "r"(xv[m].x), "r"(xv[m].y), "r"(xv[m].z), "r"(xv[m].w)
                              : "memory");
-            if (it + 1 < ncl) load_x(it + 1, xv);
+            if (it + kProd < ncl) load_x(it + kProd, xv);
             __syncwarp();
             // B fragments: 16 items per x row, each two 16-byte reads -> two entries
 #pragma unroll
             for (int u = 0; u < MP / 2; ++u) {
+                if (MP == 8 && 2 * u >= M) break;
                 const int e = lane + 32 * u;
                 const int i16 = e & 15, m = e >> 4;
                 int base, pp0, ts;
                 F::xitem(i16, base, pp0, ts);
-                const uint4 vl = lds128(xraw_a + (uint32_t)(m * 512 + base * 2));
-                const uint4 vh = lds128(xraw_a + (uint32_t)(m * 512 + (base + F::kHO) * 2));
+                const uint4 vl = lds128(xr_a + (uint32_t)(m * 512 + base * 2));
+                const uint4 vh = lds128(xr_a + (uint32_t)(m * 512 + (base + F::kHO) * 2));
                 const uint32_t d = st + SL::kB + (uint32_t)(((pp0 * MP + m) * 4 + ts) * 16);
                 asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(d), "r"(__byte_perm(vl.x, vh.x, 0x5410)),
                              "r"(__byte_perm(vl.x, vh.x, 0x7632)), "r"(__byte_perm(vl.y, vh.y, 0x5410)),
@@ -322,7 +340,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
                     for (int ch = 0; ch < NCH; ++ch) {
                         const int j = ch * IPC + ((IPC == 2 && g >= 4) ? 1 : 0);
                         const int mi = j * MPG + i;
-                        const uint4 b = lds128(st + SL::kB + (uint32_t)((((mi >> 1) * MP + (g & (MP - 1))) * 4 + t) * 16));
+                        const uint4 b = lds128(st + SL::kB + (uint32_t)((((mi >> 1) * MP + bcol) * 4 + t) * 16));
                         mma_k16(d[ch], a0, 0u, a2, 0u, b.x, b.y);
                         mma_k16(d[ch], a0n, 0u, a2n, 0u, b.z, b.w);
                     }
@@ -357,18 +375,20 @@ __global__ void __launch_bounds__(kThreadsT, 2)
                                  : "memory");
             }
             mbar_arrive(smem_addr(&full_bar[s]));
-            done = it + 1;
-            if (++s == NST) {
-                s = 0;
-                par ^= 1u;
-            }
         }
-        // every copy this CTA issued has landed before anyone leaves (each
-        // issued stage was also prepared, so its barrier can complete)
+        // every copy this CTA issued has landed before anyone leaves.  Only a
+        // stage's last copy can still be in flight (each earlier one was
+        // consumed before the stage was refilled), and each issued stage was
+        // also prepared, so its barrier can complete: once both producers have
+        // stopped issuing, each waits for the stages it filled last
+        asm volatile("bar.sync 1, %0;" ::"n"(kProd * 32) : "memory");
         if (lane == 0) {
-            for (int it = max(0, done - NST); it < done; ++it)
-                wait_bounded(smem_addr(&full_bar[it % NST]), (it / NST) & 1, kDrainWaitNs);
-            if (ncl > 0) wait_bounded(smem_addr(&sc_bar), 0, kDrainWaitNs);
+            for (int s = 0; s < NST; ++s) {
+                const int li = last_it[s];
+                if (li >= 0 && li % kProd == pw)
+                    wait_bounded(smem_addr(&full_bar[s]), (uint32_t)(li / NST) & 1u, kDrainWaitNs);
+            }
+            if (pw == 0 && ncl > 0) wait_bounded(smem_addr(&sc_bar), 0, kDrainWaitNs);
         }
         __syncwarp();
         if (S > 1) {
@@ -391,7 +411,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     const uint32_t R8S = (uint32_t)(8 * p.BX * 2);
     uint32_t sq = sc_a + (uint32_t)((rb * p.BX + g0 - gx) * 2);
     uint32_t bqb = bi_a + (uint32_t)((rb * p.BX + g0 - gx + jb) * 2);
-    const uint32_t bqo = (uint32_t)(SL::kB + (((g & (MP - 1)) * 4) + t) * 16);
+    const uint32_t bqo = (uint32_t)(SL::kB + ((bcol * 4) + t) * 16);
     const uint32_t cxo = (uint32_t)(SL::kCx + 8 * t);
     const uint32_t sxo = (uint32_t)(SL::kSx + (g * 4 + t) * 4);
     // words of group j that a thread unpacks (per row): GS/64 for 2-bit, one for 1-bit
@@ -544,7 +564,7 @@ struct TPlan {
 template <int FMT, int GS, bool HAS_BIAS, int MP>
 size_t tma_smem(int S, int stages, int RS, int BX)
 {
-    return 1024 + (size_t)stages * Stage<FMT, GS, HAS_BIAS, MP>::kBytes + kXRawBytes +
+    return 1024 + (size_t)stages * Stage<FMT, GS, HAS_BIAS, MP>::kBytes + kProd * kXRawBytes<MP> +
            (size_t)kRowsC * BX * 2 * (HAS_BIAS ? 2 : 1) + (size_t)S * RS * 8 * 4;
 }
 
