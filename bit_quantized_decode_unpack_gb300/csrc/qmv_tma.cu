@@ -93,11 +93,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-__device__ __forceinline__ void st_cluster_v2(uint32_t local_addr, uint32_t rank, float a, float b)
+// two floats into CTA `rank`'s shared memory; the write completes 8 bytes
+// of that CTA's mbarrier at the same local offset as `local_bar`
+__device__ __forceinline__ void st_async_v2(uint32_t local_addr, uint32_t local_bar, uint32_t rank, float a, float b)
 {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(a), "f"(b) : "memory");
+    uint32_t ra, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(local_bar), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(ra),
+                 "f"(a), "f"(b), "r"(rb)
+                 : "memory");
 }
 
 // mma.sync without `volatile`, so that the compiler may schedule it freely
@@ -190,6 +195,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     constexpr uint32_t CB = F::kChunkBytes;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStagesT], empty_bar[kMaxStagesT], sc_bar;
+    __shared__ __align__(8) uint64_t red_bar;  // split K: this rank's rows of every rank's partials have landed
     __shared__ int last_it[kMaxStagesT];  // iteration whose weights a stage received last (-1: none)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -213,9 +219,6 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     // runs: it prefetches its own weights and waits (griddepcontrol.wait) for
     // this grid to finish before it touches activations or outputs.
     pdl_launch_dependents();
-    // split phase: every CTA of the cluster has started before any
-    // distributed-shared-memory store (the matching wait is before them)
-    if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t ring_a = smem_addr(smem);
@@ -234,9 +237,19 @@ __global__ void __launch_bounds__(kThreadsT, 2)
             mbar_init(smem_addr(&empty_bar[s]), kCons * 32);
         }
         mbar_init(smem_addr(&sc_bar), 1);
+        if (S > 1) {
+            // rows [rank RS, rank RS + nrow) from all S ranks, ceil(M/2) float pairs a row
+            const int nrow = min(p.RS, kRowsC - rank * p.RS);
+            mbar_init(smem_addr(&red_bar), 1);
+            mbar_arrive_expect_tx(smem_addr(&red_bar), (uint32_t)(S * nrow * ((M + 1) / 2) * 8));
+        }
     }
     if (tid < kMaxStagesT) last_it[tid] = -1;
     __syncthreads();
+    // split phase: every CTA of the cluster has started, with its reduction
+    // barrier set up, before any distributed-shared-memory store (the matching
+    // wait is before them)
+    if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     uint32_t mg[10];
 #pragma unroll
     for (int i = 0; i < 10; ++i) mg[i] = F::magic_at(i < F::kNumMagic ? i : 0) ^ p.zero;
@@ -393,7 +406,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         __syncwarp();
         if (S > 1) {
             asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-            asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+            asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
         }
         return;
     }
@@ -515,19 +528,29 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         return;
     }
     // reduce-scatter through distributed shared memory: rank q adds rows
-    // [q RS, (q+1) RS) of every rank's partials, in rank order
+    // [q RS, (q+1) RS) of every rank's partials, in rank order.  Each rank
+    // sends its column pairs below M with st.async, which completes bytes of
+    // the receiving rank's red_bar; a rank reads its rows once all have
+    // landed.  The cluster barrier split around the reduction keeps every CTA
+    // resident until every rank has received all of its rows.
     const int RS = p.RS;
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    if (2 * t < M) {
+        const uint32_t rbar = smem_addr(&red_bar);
 #pragma unroll
-    for (int tl = 0; tl < 2; ++tl)
+        for (int tl = 0; tl < 2; ++tl)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int row = rb + 16 * tl + 8 * h;
-            const int q = row / RS;
-            st_cluster_v2(smem_addr(red + ((size_t)rank * RS + (row - q * RS)) * 8 + 2 * t), (uint32_t)q,
-                          acc[tl][2 * h], acc[tl][2 * h + 1]);
-        }
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+            for (int h = 0; h < 2; ++h) {
+                const int row = rb + 16 * tl + 8 * h;
+                const int q = row / RS;
+                st_async_v2(smem_addr(red + ((size_t)rank * RS + (row - q * RS)) * 8 + 2 * t), rbar, (uint32_t)q,
+                            acc[tl][2 * h], acc[tl][2 * h + 1]);
+            }
+    }
+    // every rank sends all of its rows whatever its own waits did, so this
+    // wait keeps the long limit of the drains
+    wait_bounded(smem_addr(&red_bar), 0, kDrainWaitNs);
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     const int row0 = rank * RS;
     const int nrow = min(RS, kRowsC - row0);
     for (int e = tid; e < nrow * M; e += kCons * 32) {
@@ -537,6 +560,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         const int n = n0 + row0 + lr;
         if (n < p.N) outg[(size_t)m * p.N + n] = __float2half_rn(v);
     }
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // ---- host side -------------------------------------------------------------------------
