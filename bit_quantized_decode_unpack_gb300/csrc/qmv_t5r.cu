@@ -253,11 +253,25 @@ __device__ __forceinline__ void mma_r(float (&c)[4], uint32_t a0, uint32_t a1, u
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void st_cluster_v2r(uint32_t local_addr, uint32_t rank, float a, float b)
+// one or two floats into CTA `rank`'s shared memory; each write completes
+// its bytes on that CTA's mbarrier at the same local offset as `local_bar`
+__device__ __forceinline__ void st_async_f32r(uint32_t local_addr, uint32_t local_bar, uint32_t rank, float a)
 {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(a), "f"(b) : "memory");
+    uint32_t ra, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(local_bar), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(ra), "f"(a), "r"(rb)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_v2r(uint32_t local_addr, uint32_t local_bar, uint32_t rank, float a, float b)
+{
+    uint32_t ra, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(local_bar), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(ra),
+                 "f"(a), "f"(b), "r"(rb)
+                 : "memory");
 }
 
 // fp16x2 constants of the decode (in registers)
@@ -332,6 +346,7 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
     constexpr int MPG = Ge::MPG;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStagesR], empty_bar[kMaxStagesR], x_bar[2];
+    __shared__ __align__(8) uint64_t red_bar;  // split K: this rank's rows of every rank's partials have landed
     __shared__ __align__(16) uint16_t koff[kPairsR * 4 * 8];  // (pair, slot, half) -> staging offset
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -348,9 +363,6 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
     // the next kernel may launch now: it only prefetches its weights until
     // its griddepcontrol.wait, which waits for this whole grid
     pdl_launch_dependents();
-    // split phase: every CTA of the cluster has started before any
-    // distributed-shared-memory store (the matching wait is before them)
-    if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t ring_a = smem_addr(smem);
@@ -380,12 +392,24 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
         }
         mbar_init(smem_addr(&x_bar[0]), 1);
         mbar_init(smem_addr(&x_bar[1]), 1);
+        if (S > 1) {
+            // rows [rank RS, rank RS + nrow) from all S ranks: M floats a row
+            // (column split), else ceil(M/2) float pairs
+            const int nrow = min(p.RS, kRowsR - rank * p.RS);
+            const int row_bytes = COL ? 4 * M : 8 * ((M + 1) / 2);
+            mbar_init(smem_addr(&red_bar), 1);
+            mbar_arrive_expect_tx(smem_addr(&red_bar), (uint32_t)(S * nrow * row_bytes));
+        }
     }
     if constexpr (COL) {
         for (int i = tid; i < 4 * NST; i += kThreadsR)
             sts128(ring_a + (uint32_t)(i >> 2) * STB + (uint32_t)(SL::zero_off(M) + (i & 3) * 16), make_uint4(0, 0, 0, 0));
     }
     __syncthreads();
+    // split phase: every CTA of the cluster has started, with its reduction
+    // barrier set up, before any distributed-shared-memory store (the matching
+    // wait is before them)
+    if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     if (warp == NW) {
         // ---- producer ----------------------------------------------------------------
@@ -562,7 +586,7 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
         __syncwarp();
         if (S > 1) {
             asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-            asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+            asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
         }
         return;
     }
@@ -773,22 +797,30 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
         }
         return;
     }
+    // reduce-scatter: each rank sends its values with st.async, completing
+    // bytes of the receiving rank's red_bar; a rank adds its rows once all
+    // have landed.  The cluster barrier split around the reduction keeps
+    // every CTA resident until every rank has received all of its rows.
     const int RS = p.RS;
+    const uint32_t rbar = smem_addr(&red_bar);
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     if constexpr (COL) {
         const int row = r0 + 8 * rr_t;
         const int q = row / RS;
-        if (e_t < M) st_cluster_f32(smem_addr(red + ((size_t)rank * RS + (row - q * RS)) * 8 + e_t), (uint32_t)q, vcol);
-    } else {
+        if (e_t < M) st_async_f32r(smem_addr(red + ((size_t)rank * RS + (row - q * RS)) * 8 + e_t), rbar, (uint32_t)q, vcol);
+    } else if (2 * t < M) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int row = r0 + 8 * h;
             const int q = row / RS;
-            st_cluster_v2r(smem_addr(red + ((size_t)rank * RS + (row - q * RS)) * 8 + 2 * t), (uint32_t)q, v[2 * h],
-                           v[2 * h + 1]);
+            st_async_v2r(smem_addr(red + ((size_t)rank * RS + (row - q * RS)) * 8 + 2 * t), rbar, (uint32_t)q, v[2 * h],
+                         v[2 * h + 1]);
         }
     }
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    // every rank sends all of its rows whatever its own waits did, so this
+    // wait keeps the long limit of the drains
+    wait_bounded_r(rbar, 0, kDrainWaitNs);
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     const int row0 = rank * RS;
     const int nrow = min(RS, kRowsR - row0);
     for (int i = tid; i < nrow * M; i += NW * 32) {
@@ -798,6 +830,7 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
         const int n = n0 + row0 + lr;
         if (n < p.N && m < Mv) outg[(size_t)m * p.N + n] = __float2half_rn(sum);
     }
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // ---- host side -----------------------------------------------------------------------------
