@@ -186,13 +186,14 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c)
 // NH = 2: the CTA owns two 256-column blocks of x (two N=256 accumulators,
 // all 512 TMEM columns), so each decoded weight tile serves 512 columns; its
 // K step is then 64 codes (half a 128-group), which keeps two stages of
-// [A 16 KB | X 64 KB] in shared memory.  1/2-bit, and t5 at gs=64 (a 128-code
-// t5 group cannot be split into byte-aligned 32-code quarters).
+// [A 16 KB | X 64 KB] in shared memory.  A 128-code t5 group is then decoded
+// in quarters of 32 codes that start inside bytes 0, 6, 12 and 18 of its 26
+// (codes 0, 32, 64 and 96 are digits 0, 2, 4 and 1 of those bytes).
 template <int FMT, int GS, int NH>
 __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParams &p)
 {
     constexpr bool T5F = FMT == BQD_FMT_T5;
-    static_assert(NH == 1 || (NH == 2 && (!T5F || GS == 64)), "two column blocks: 1/2-bit or t5 at gs=64");
+    static_assert(NH == 1 || NH == 2, "one or two column blocks");
     constexpr int KS = NH == 2 ? 64 : GS;  // codes per K step
     constexpr int SPG = GS / KS;           // K steps per group (1 or 2)
     constexpr int B = GS == 64 ? 13 : 26;  // t5 bytes per group
@@ -328,8 +329,11 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
         // t5: the bytes of this thread's half of the group, from byte FB (0, or
         // 12 / 6 for the second half), NWH words, read as two aligned 16-byte
         // loads (row_bytes is a multiple of 16 here) and realigned in registers.
-        constexpr int FB1 = GS == 128 ? 12 : 6;
-        constexpr int NWH = GS == 128 ? 4 : 2;
+        // (two-block gs=128: a quarter's bytes start at 0 / 12 for h = 0 and
+        // 6 / 18 for h = 1 in even / odd K steps, and span at most 8 bytes)
+        constexpr bool Q4 = T5F && GS == 128 && NH == 2;
+        constexpr int FB1 = GS == 128 && !Q4 ? 12 : 6;
+        constexpr int NWH = GS == 128 && !Q4 ? 4 : 2;
         // 1/2-bit: half h of a K step is HB bytes (HW words) at byte
         // (first code of the step)/CPB + h*HB, one aligned load (row_bytes is
         // a multiple of 2HB and the base is 16-byte aligned)
@@ -348,10 +352,16 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
         const uint8_t *wp = wrow + (long long)g_lo * (GS / CPB) + h * HB;
         const __half *sp = srow + g_lo, *bp = brow ? brow + g_lo : nullptr;
         int sstep = 0;  // K steps fetched in the current group (SPG per group)
+        int fpar = 0;   // quarters: parity of the K step being fetched
         auto fetch = [&]() {
             if constexpr (T5F) {
                 const long long start = t5_start;
-                t5_start += B;
+                if constexpr (Q4) {
+                    t5_start += fpar ? 14 : 12;
+                    fpar ^= 1;
+                } else {
+                    t5_start += B;
+                }
                 const long long astart = start & ~15LL;
                 ow_n = (int)(start & 15);
                 w0n = rok ? *reinterpret_cast<const uint4 *>(wrow + astart) : make_uint4(0, 0, 0, 0);
@@ -449,7 +459,16 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
                     out[0] = wv(u, 0x00030003u, 0);
                     out[1] = wv(u, 0x00300030u, 2);
                 };
-                if (GS == 128) {
+                if (Q4 && (it & 1)) {
+                    // odd K step: codes 64..127 of the group.  The four byte pairs
+                    // from the fetched byte give codes 60..99 (h = 0, byte 12) or
+                    // 90..129 (h = 1, byte 18); the quarter starts at word 2 / 3
+                    uint32_t tmp[20];
+#pragma unroll
+                    for (int jp = 0; jp < 4; ++jp) pair_at(2 * jp, &tmp[5 * jp]);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) hv[i] = h ? tmp[i + 3] : tmp[i + 2];
+                } else if (GS == 128 && !Q4) {
                     if (h == 0) {  // codes 0..63: byte pairs (0,1) .. (10,11), then byte 12's first four
 #pragma unroll
                         for (int jp = 0; jp < 6; ++jp) pair_at(2 * jp, &hv[5 * jp]);
@@ -462,6 +481,8 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
                         for (int i = 0; i < 32; ++i) hv[i] = tmp[i + 2];
                     }
                 } else {
+                    // a 64-code group, or the even K step of a two-block gs=128
+                    // group (codes 0..63, laid out as a 64-code group's)
                     if (h == 0) {  // codes 0..31: byte pairs (0,1) .. (4,5), then byte 6's first two
                         uint32_t tmp[17];
 #pragma unroll
@@ -753,11 +774,11 @@ int launch_qmm(const QmvArgs &a, cudaStream_t s)
     p.wait_ns = (unsigned long long)opt_wait_ns();
     p.zero = 0;
     p.bx = a.M <= 32 ? 32 : (a.M <= 64 ? 64 : (a.M <= 128 ? 128 : 256));
-    // 1/2-bit (and t5 at gs=64) with more than 256 x rows on a wide layer: two
+    // more than 256 x rows on a wide layer: two
     // 256-column blocks per CTA (the decoded weight tile serves 512 columns),
     // K steps of 64 codes.  Narrow layers keep one block: their few 128-row tiles would
     // leave SMs idle (measured: down projection, M=512, 813 -> 470 TFLOP/s)
-    const bool pair = (a.fmt != BQD_FMT_T5 || a.gs == 64) && a.M > 256 && a.N >= 8192;
+    const bool pair = a.M > 256 && a.N >= 8192;
     const int NH = pair ? 2 : 1;
     const int KS = pair ? 64 : a.gs;
     const int cols = NH * p.bx;
@@ -791,7 +812,9 @@ int launch_qmm(const QmvArgs &a, cudaStream_t s)
         fprintf(stderr, "bqd qmm plan: fmt=%d M=%d N=%d K=%d gs=%d -> bx=%d x%d tiles=%d S=%d gpr=%d stages=%d smem=%zu\n",
                 a.fmt, p.M, p.N, p.K, a.gs, p.bx, NH, tiles, S, p.gpr, p.stages, smem);
     if (a.fmt == BQD_FMT_T5) {
-        if (pair) return launch_gs<BQD_FMT_T5, 64, 2>(p, map, tiles, smem, s);
+        if (pair)
+            return a.gs == 64 ? launch_gs<BQD_FMT_T5, 64, 2>(p, map, tiles, smem, s)
+                              : launch_gs<BQD_FMT_T5, 128, 2>(p, map, tiles, smem, s);
         return a.gs == 64 ? launch_gs<BQD_FMT_T5, 64, 1>(p, map, tiles, smem, s)
                           : launch_gs<BQD_FMT_T5, 128, 1>(p, map, tiles, smem, s);
     }

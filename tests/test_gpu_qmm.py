@@ -142,13 +142,17 @@ def test_affine_two_column_blocks_per_cta(fmt, gs, sym):
         run(p, m_rows=m_rows, n_rows=n_rows)
 
 
+@pytest.mark.parametrize("gs", [64, 128])
 @pytest.mark.parametrize("bias", [False, True])
-def test_t5_gs64_two_column_blocks_per_cta(bias):
-    """t5 at gs=64 takes the two-block mode too (its 64-code groups split into
-    byte-aligned 32-code halves); sampled outputs as above."""
-    rng = np.random.default_rng(64 + bias)
-    for M, N, K in [(300, 8200, 1024), (513, 8192, 1024)]:
-        p = synth.problem(T5, M, N, K, 64, sym=True)
+def test_t5_two_column_blocks_per_cta(gs, bias):
+    """t5 takes the two-block mode too: a 64-code group splits into 32-code
+    halves at bytes 0 and 6, a 128-code group into quarters that start inside
+    bytes 0, 6, 12 and 18 (the product takes rows of whole 16-byte pieces, so
+    K / gs is a multiple of 16 at gs=64 and of 8 at gs=128).  Sampled outputs
+    as above."""
+    rng = np.random.default_rng(gs + bias)
+    for M, N, K in [(300, 8200, 1024), (513, 8192, 3072)]:
+        p = synth.problem(T5, M, N, K, gs, sym=True)
         if bias:
             p["biases"] = synth.biases(rng, F2, p["scales"])
         m_rows = np.unique(np.concatenate([[0, 255, 256, M - 1], rng.integers(0, M, 12)]))
@@ -217,6 +221,31 @@ def test_affine_one_hot_x_recovers_the_weights(fmt):
     b = p["biases"][:, ks // gs].astype(np.float32)
     q = p["codes"][:, ks].astype(np.float32)
     want = ((s * q).astype(np.float16).astype(np.float32) + b).astype(np.float16).T
+    assert np.array_equal(y.cpu().numpy().view(np.int16), want.view(np.int16))
+
+
+@pytest.mark.parametrize("gs", [64, 128])
+def test_t5_two_column_blocks_one_hot_x_recovers_the_weights(gs):
+    """Two-block mode (M > 256, N >= 8192), x = e_k with k = m mod K: every
+    code position of every half / quarter pattern comes back as the
+    dequantised weight fp16(fp16(s*t) + b), bit for bit."""
+    import torch
+    M, N, K = 300, 8192, 1024  # k = 0 .. 299: all of the first two 128-code groups
+    rng = np.random.default_rng(7 + gs)
+    p = synth.problem(T5, M, N, K, gs, sym=True)
+    p["biases"] = synth.biases(rng, F2, p["scales"])
+    ks = np.arange(M) % K
+    x = np.zeros((M, K), dtype=np.float16)
+    x[np.arange(M), ks] = 1.0
+    w = bqd.pack(to_dev(p["codes"]), T5, gs)
+    with forced_kernel("qmm"):
+        y = bqd.qmv(to_dev(x), w, to_dev(p["scales"]), to_dev(p["biases"]), T5, gs)
+    torch.cuda.synchronize()
+    assert bqd.device_status() == 0
+    s = p["scales"][:, ks // gs].astype(np.float32)            # [N, M]
+    b = p["biases"][:, ks // gs].astype(np.float32)
+    t = p["codes"][:, ks].astype(np.float32)
+    want = ((s * t).astype(np.float16).astype(np.float32) + b).astype(np.float16).T
     assert np.array_equal(y.cpu().numpy().view(np.int16), want.view(np.int16))
 
 
