@@ -45,6 +45,7 @@
 #include <stdio.h>
 #include <stdlib.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "bqd_internal.cuh"
@@ -114,6 +115,15 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
 __device__ __forceinline__ void tc_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t local_addr, uint32_t rank, uint32_t a, uint32_t b, uint32_t c,
+                                              uint32_t d)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
 }
 
@@ -634,8 +644,17 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
     __syncthreads();
     tc_fence_after();
     const bool ok_all = !abort_flag;
-    float *red = reinterpret_cast<float *>(smem);  // split-K partials reuse rank 0's stage ring
-    if (S > 1) cluster_sync();                     // every rank's MMAs are complete
+    // split K: a reduce-scatter over 32-column blocks.  Rank q owns blocks
+    // [q nb / S, (q+1) nb / S) and writes their outputs; every other rank
+    // stores its partials of those blocks into q's stage ring, laid out
+    // [S-1 sources][128 rows][W_q + 4] fp32 (a row padded by 16 bytes, so that
+    // the lanes' 16-byte accesses spread over the banks), and q adds the S
+    // partials in rank order.
+    const int nb = C / 32;
+    const int lo_me = rank * nb / S, hi_me = (rank + 1) * nb / S;
+    const int wst_me = (hi_me - lo_me) * 32 + 4;
+    float *red = reinterpret_cast<float *>(smem);
+    if (S > 1) cluster_sync();  // every rank's MMAs are complete: the rings are free
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const int row = n0 + r;
@@ -643,18 +662,27 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
     const int cw = C >= 64 ? C / 2 : C;
     const int c_beg = C >= 64 ? (warp >> 2) * cw : 0;
     const bool drains = warp < kDecodeWarpsQ && (C >= 64 || warp < 4);
-    if (drains && S > 1 && rank != 0 && steps > 0) {
+    if (drains && S > 1 && steps > 0) {
         for (int c0 = c_beg; c0 < c_beg + cw; c0 += 32) {
+            const int b = c0 >> 5;
+            int q = 0;
+            while ((q + 1) * nb / S <= b) ++q;  // the owner: lo_q <= b < hi_q
+            if (q == rank) continue;
+            const int lo_q = q * nb / S, hi_q = (q + 1) * nb / S;
+            const int wst = (hi_q - lo_q) * 32 + 4;
+            const int slot = rank < q ? rank : rank - 1;
             uint32_t v[32];
             tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)c0, v);
-            float *dst = red + ((size_t)(rank - 1) * 128 + r) * C + c0;
+            const uint32_t dst = smem_addr(red + ((size_t)slot * 128 + r) * wst + (b - lo_q) * 32);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) st_cluster_f32(smem_addr(dst + q), 0, __uint_as_float(v[q]));
+            for (int j = 0; j < 32; j += 4) st_cluster_v4(dst + 4 * j, (uint32_t)q, v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
     }
     if (S > 1) cluster_sync();
-    if (drains && rank == 0 && ok_all) {
+    if (drains && ok_all) {
         for (int c0 = c_beg; c0 < c_beg + cw; c0 += 32) {
+            const int b = c0 >> 5;
+            if (b < lo_me || b >= hi_me) continue;
             uint32_t v[32];
             if (steps > 0) {
                 tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)c0, v);
@@ -662,13 +690,30 @@ __device__ __forceinline__ void qmm_body(const CUtensorMap &xmap, const QmmParam
 #pragma unroll
                 for (int q = 0; q < 32; ++q) v[q] = 0u;
             }
+            float acc[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) acc[q] = 0.f;
+            for (int src = 0; src < S; ++src) {
+                if (src == rank) {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) acc[q] += __uint_as_float(v[q]);
+                } else if (src * p.gpr < p.G) {  // ranks without groups sent nothing
+                    const int slot = src < rank ? src : src - 1;
+                    const float *rp = red + ((size_t)slot * 128 + r) * wst_me + (b - lo_me) * 32;
+#pragma unroll
+                    for (int q = 0; q < 32; q += 4) {
+                        const float4 t4 = *reinterpret_cast<const float4 *>(rp + q);
+                        acc[q] += t4.x;
+                        acc[q + 1] += t4.y;
+                        acc[q + 2] += t4.z;
+                        acc[q + 3] += t4.w;
+                    }
+                }
+            }
 #pragma unroll
             for (int q = 0; q < 32; ++q) {
-                float acc = __uint_as_float(v[q]);
-                for (int rr = 1; rr < S; ++rr)
-                    if (rr * p.gpr < p.G) acc += red[((size_t)(rr - 1) * 128 + r) * C + c0 + q];
                 const int m = m0 + c0 + q;
-                if (row < p.N && m < p.M) p.out[(size_t)m * p.N + row] = __float2half_rn(acc);
+                if (row < p.N && m < p.M) p.out[(size_t)m * p.N + row] = __float2half_rn(acc[q]);
             }
         }
     }
@@ -708,10 +753,48 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-template <int FMT, int GS, int NH>
-int launch_gs(const QmmParams &p, const CUtensorMap &map, int tiles, size_t smem, cudaStream_t s)
+using QmmKernel = void (*)(const CUtensorMap, const QmmParams);
+
+// clusters of S CTAs (CTAs for S = 1) that can be resident at once
+int qmm_slots(QmmKernel kern, int S, size_t smem)
 {
-    void (*kern)(const CUtensorMap, const QmmParams);
+    struct Entry { int dev; QmmKernel kern; int S; size_t smem; int slots; };
+    static Entry cache[64];
+    static int n = 0;
+    static std::mutex mu;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+        if (cache[i].dev == dev && cache[i].kern == kern && cache[i].S == S && cache[i].smem == smem) return cache[i].slots;
+    int slots = 0;
+    if (S == 1) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreadsQ, smem) == cudaSuccess)
+            slots = per_sm * sm_count();
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(S * 16);
+        cfg.blockDim = dim3(kThreadsQ);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = S;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&slots, kern, &cfg) != cudaSuccess) slots = 0;
+    }
+    cudaGetLastError();
+    if (n < 64) cache[n++] = Entry{dev, kern, S, smem, slots};
+    return slots;
+}
+
+template <int FMT, int GS, int NH>
+int launch_gs(QmmParams p, const CUtensorMap &map, int tiles, size_t per_stage, int cols, cudaStream_t s)
+{
+    QmmKernel kern;
     if constexpr (FMT == BQD_FMT_T5)
         kern = qmm_t5_kernel<GS, NH>;
     else
@@ -724,6 +807,27 @@ int launch_gs(const QmmParams &p, const CUtensorMap &map, int tiles, size_t smem
             return BQD_ERR_CUDA;
         configured_dev[dev] = 1;
     }
+    const size_t smem = (size_t)p.stages * per_stage + 1024;
+    // Split K over a cluster of S CTAs while every cluster of the grid is
+    // resident at once (occupancy query), each rank keeps >= 4 groups, and the
+    // partials a rank receives fit its stage ring.  (A split that needs more
+    // than one wave measured slower: narrow layers at M = 512 and 2048 lost
+    // 0-10% with S = 4-5 over two or three waves against S = 1.)
+    const int nb = cols / 32;
+    int bestS = 1;
+    for (int S = 2; S <= 8; ++S) {
+        if (p.G < 4 * S) break;
+        int wmax = 0;
+        for (int q = 0; q < S; ++q) wmax = std::max(wmax, ((q + 1) * nb / S - q * nb / S) * 32);
+        if ((size_t)(S - 1) * 128 * (wmax + 4) * 4 > (size_t)p.stages * per_stage) break;
+        if (tiles > qmm_slots(kern, S, smem)) break;
+        bestS = S;
+    }
+    p.S = bestS;
+    p.gpr = (p.G + bestS - 1) / bestS;
+    if (opt_debug_plan())
+        fprintf(stderr, "bqd qmm plan: fmt=%d M=%d N=%d K=%d gs=%d -> bx=%d x%d tiles=%d S=%d gpr=%d stages=%d smem=%zu\n",
+                FMT, p.M, p.N, p.K, GS, p.bx, NH, tiles, p.S, p.gpr, p.stages, smem);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tiles * p.S);
     cfg.blockDim = dim3(kThreadsQ);
@@ -774,31 +878,20 @@ int launch_qmm(const QmvArgs &a, cudaStream_t s)
     p.wait_ns = (unsigned long long)opt_wait_ns();
     p.zero = 0;
     p.bx = a.M <= 32 ? 32 : (a.M <= 64 ? 64 : (a.M <= 128 ? 128 : 256));
-    // more than 256 x rows on a wide layer: two
-    // 256-column blocks per CTA (the decoded weight tile serves 512 columns),
-    // K steps of 64 codes.  Narrow layers keep one block: their few 128-row tiles would
-    // leave SMs idle (measured: down projection, M=512, 813 -> 470 TFLOP/s)
+    // more than 256 x rows on a wide layer: two 256-column blocks per CTA (the
+    // decoded weight tile serves 512 columns), K steps of 64 codes.  Narrow
+    // layers keep one block: their few 128-row tiles would leave SMs idle
+    // (measured: down projection, M=512, 813 -> 470 TFLOP/s)
     const bool pair = a.M > 256 && a.N >= 8192;
     const int NH = pair ? 2 : 1;
     const int KS = pair ? 64 : a.gs;
     const int cols = NH * p.bx;
     const int n_tiles = (p.N + 127) / 128, m_tiles = (p.M + cols - 1) / cols;
     const int tiles = n_tiles * m_tiles;
-    const int sms = sm_count();
     const size_t per_stage = (size_t)128 * KS * 2 + (size_t)cols * KS * 2;
     p.stages = (int)((kQmmSmemMax - 1024) / per_stage);
     if (p.stages > kMaxStagesQ) p.stages = kMaxStagesQ;
     if (p.stages < 2) return BQD_ERR_UNSUPPORTED;
-    // split K over a cluster while that fills more SMs (one CTA per SM), each
-    // rank keeps >= 4 groups, and the (S-1) fp32 partial tiles fit the ring
-    int S = 1;
-    while (S < 8 && tiles * (S + 1) <= sms && p.G >= 4 * (S + 1) &&
-           (size_t)S * 128 * cols * 4 <= (size_t)p.stages * per_stage)
-        ++S;
-    p.S = S;
-    p.gpr = (p.G + S - 1) / S;
-    const size_t smem = (size_t)p.stages * per_stage + 1024;
-
     CUtensorMap map;
     cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
     cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
@@ -808,28 +901,25 @@ int launch_qmm(const QmvArgs &a, cudaStream_t s)
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return BQD_ERR_CUDA;
-    if (opt_debug_plan())
-        fprintf(stderr, "bqd qmm plan: fmt=%d M=%d N=%d K=%d gs=%d -> bx=%d x%d tiles=%d S=%d gpr=%d stages=%d smem=%zu\n",
-                a.fmt, p.M, p.N, p.K, a.gs, p.bx, NH, tiles, S, p.gpr, p.stages, smem);
     if (a.fmt == BQD_FMT_T5) {
         if (pair)
-            return a.gs == 64 ? launch_gs<BQD_FMT_T5, 64, 2>(p, map, tiles, smem, s)
-                              : launch_gs<BQD_FMT_T5, 128, 2>(p, map, tiles, smem, s);
-        return a.gs == 64 ? launch_gs<BQD_FMT_T5, 64, 1>(p, map, tiles, smem, s)
-                          : launch_gs<BQD_FMT_T5, 128, 1>(p, map, tiles, smem, s);
+            return a.gs == 64 ? launch_gs<BQD_FMT_T5, 64, 2>(p, map, tiles, per_stage, cols, s)
+                              : launch_gs<BQD_FMT_T5, 128, 2>(p, map, tiles, per_stage, cols, s);
+        return a.gs == 64 ? launch_gs<BQD_FMT_T5, 64, 1>(p, map, tiles, per_stage, cols, s)
+                          : launch_gs<BQD_FMT_T5, 128, 1>(p, map, tiles, per_stage, cols, s);
     }
     if (a.fmt == BQD_FMT_AFFINE2) {
         if (pair)
-            return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE2, 64, 2>(p, map, tiles, smem, s)
-                              : launch_gs<BQD_FMT_AFFINE2, 128, 2>(p, map, tiles, smem, s);
-        return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE2, 64, 1>(p, map, tiles, smem, s)
-                          : launch_gs<BQD_FMT_AFFINE2, 128, 1>(p, map, tiles, smem, s);
+            return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE2, 64, 2>(p, map, tiles, per_stage, cols, s)
+                              : launch_gs<BQD_FMT_AFFINE2, 128, 2>(p, map, tiles, per_stage, cols, s);
+        return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE2, 64, 1>(p, map, tiles, per_stage, cols, s)
+                          : launch_gs<BQD_FMT_AFFINE2, 128, 1>(p, map, tiles, per_stage, cols, s);
     }
     if (pair)
-        return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE1, 64, 2>(p, map, tiles, smem, s)
-                          : launch_gs<BQD_FMT_AFFINE1, 128, 2>(p, map, tiles, smem, s);
-    return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE1, 64, 1>(p, map, tiles, smem, s)
-                      : launch_gs<BQD_FMT_AFFINE1, 128, 1>(p, map, tiles, smem, s);
+        return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE1, 64, 2>(p, map, tiles, per_stage, cols, s)
+                          : launch_gs<BQD_FMT_AFFINE1, 128, 2>(p, map, tiles, per_stage, cols, s);
+    return a.gs == 64 ? launch_gs<BQD_FMT_AFFINE1, 64, 1>(p, map, tiles, per_stage, cols, s)
+                      : launch_gs<BQD_FMT_AFFINE1, 128, 1>(p, map, tiles, per_stage, cols, s);
 }
 
 }  // namespace bqd
