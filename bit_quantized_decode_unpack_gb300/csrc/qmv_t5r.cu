@@ -253,6 +253,28 @@ __device__ __forceinline__ void mma_r(float (&c)[4], uint32_t a0, uint32_t a1, u
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// (a0, a1) = fma(s, (d0 + e0, d1 + e1) - (c0, c1), fma(b, (x0, x1), (a0, a1)))
+// on packed fp32 pairs: each element rounds as the scalar operations would
+__device__ __forceinline__ void col_epi2(float &a0, float &a1, float s, float b, float d0, float d1, float e0, float e1,
+                                         float c0, float c1, float x0, float x1)
+{
+    asm("{\n\t.reg .b64 d, e, c, x, a, ss, bb;\n\t"
+        "mov.b64 d, {%2, %3};\n\t"
+        "mov.b64 e, {%4, %5};\n\t"
+        "mov.b64 c, {%6, %7};\n\t"
+        "mov.b64 x, {%8, %9};\n\t"
+        "mov.b64 ss, {%10, %10};\n\t"
+        "mov.b64 bb, {%11, %11};\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "add.rn.f32x2 d, d, e;\n\t"
+        "sub.rn.f32x2 d, d, c;\n\t"
+        "fma.rn.f32x2 a, bb, x, a;\n\t"
+        "fma.rn.f32x2 a, ss, d, a;\n\t"
+        "mov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(d0), "f"(d1), "f"(e0), "f"(e1), "f"(c0), "f"(c1), "f"(x0), "f"(x1), "f"(s), "f"(b));
+}
+
 // one or two floats into CTA `rank`'s shared memory; each write completes
 // its bytes on that CTA's mbarrier at the same local offset as `local_bar`
 __device__ __forceinline__ void st_async_f32r(uint32_t local_addr, uint32_t local_bar, uint32_t rank, float a)
@@ -680,11 +702,11 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
                 const uint4 v = lds128r(st_a + (uint32_t)SL::sx_off(M) + (uint32_t)((P * 4 + t) * 16));
                 const float sx[2] = {__uint_as_float(v.x), __uint_as_float(v.z)};
                 const float cx[2] = {__uint_as_float(v.y), __uint_as_float(v.w)};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int rr = q >> 1, e = q & 1;
-                    acc[0][q] = fmaf(sc[rr], (d2[0][q] + d2[1][q]) - cx[e], fmaf(bi[rr], sx[e], acc[0][q]));
-                }
+                // value q: row half q >> 1 (scale and bias rr), x row q & 1
+                col_epi2(acc[0][0], acc[0][1], sc[0], bi[0], d2[0][0], d2[0][1], d2[1][0], d2[1][1], cx[0], cx[1], sx[0],
+                         sx[1]);
+                col_epi2(acc[0][2], acc[0][3], sc[1], bi[1], d2[0][2], d2[0][3], d2[1][2], d2[1][3], cx[0], cx[1], sx[0],
+                         sx[1]);
             }
         } else {
 

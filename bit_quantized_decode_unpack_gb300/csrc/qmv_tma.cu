@@ -114,6 +114,22 @@ __device__ __forceinline__ void mma_k16(float (&c)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// (a0, a1) = fma(s, (g0, g1) - (c0, c1), (a0, a1)) on packed fp32 pairs: each
+// element rounds as the scalar subtraction and fused multiply-add would
+__device__ __forceinline__ void fma_sub2(float &a0, float &a1, float s, float g0, float g1, float c0, float c1)
+{
+    asm("{\n\t.reg .b64 g, c, d, a, ss;\n\t"
+        "mov.b64 g, {%2, %3};\n\t"
+        "mov.b64 c, {%4, %5};\n\t"
+        "sub.rn.f32x2 d, g, c;\n\t"
+        "mov.b64 ss, {%6, %6};\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "fma.rn.f32x2 a, ss, d, a;\n\t"
+        "mov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(g0), "f"(g1), "f"(c0), "f"(c1), "f"(s));
+}
+
 __device__ __forceinline__ void mma_k8(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0)
 {
     asm("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
@@ -498,10 +514,8 @@ __global__ void __launch_bounds__(kThreadsT, 2)
             for (int tl = 0; tl < 2; ++tl) {
                 const float sa = (j & 1) ? h2f_hi(sw[2 * tl][j >> 1]) : h2f_lo(sw[2 * tl][j >> 1]);
                 const float sb = (j & 1) ? h2f_hi(sw[2 * tl + 1][j >> 1]) : h2f_lo(sw[2 * tl + 1][j >> 1]);
-                acc[tl][0] = fmaf(sa, ag[tl][0] - cx0, acc[tl][0]);
-                acc[tl][1] = fmaf(sa, ag[tl][1] - cx1, acc[tl][1]);
-                acc[tl][2] = fmaf(sb, ag[tl][2] - cx0, acc[tl][2]);
-                acc[tl][3] = fmaf(sb, ag[tl][3] - cx1, acc[tl][3]);
+                fma_sub2(acc[tl][0], acc[tl][1], sa, ag[tl][0], ag[tl][1], cx0, cx1);
+                fma_sub2(acc[tl][2], acc[tl][3], sb, ag[tl][2], ag[tl][3], cx0, cx1);
             }
         }
         mbar_arrive(smem_addr(&empty_bar[s]));
