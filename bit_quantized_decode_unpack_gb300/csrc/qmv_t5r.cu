@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
         if (S > 1) {
             // rows [rank RS, rank RS + nrow) from all S ranks: M floats a row
             // (column split), else ceil(M/2) float pairs
-            const int nrow = min(p.RS, kRowsR - rank * p.RS);
+            const int nrow = max(0, min(p.RS, kRowsR - rank * p.RS));
             const int row_bytes = COL ? 4 * M : 8 * ((M + 1) / 2);
             mbar_init(smem_addr(&red_bar), 1);
             mbar_arrive_expect_tx(smem_addr(&red_bar), (uint32_t)(S * nrow * row_bytes));
@@ -844,7 +844,7 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
     wait_bounded_r(rbar, 0, kDrainWaitNs);
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     const int row0 = rank * RS;
-    const int nrow = min(RS, kRowsR - row0);
+    const int nrow = max(0, min(RS, kRowsR - row0));
     for (int i = tid; i < nrow * M; i += NW * 32) {
         const int lr = i / M, m = i % M;
         float sum = 0.f;
@@ -947,6 +947,9 @@ bool plan_r(int M, int N, int chunks, int P, RPlan &best)
         const int Cs = (chunks + S - 1) / S;
         if ((S - 1) * Cs >= chunks) continue;
         const int RS = (kRowsR + S - 1) / S;
+        // every rank owns rows of the reduction (128 rows over 14 ranks would
+        // leave the last one none)
+        if ((S - 1) * RS >= kRowsR) continue;
         const size_t fixed = t5r_smem<GS, HAS_BIAS, COL, NW>(M, S, 0, RS);
         if (fixed + stage > kSmemBudgetR) continue;
         int st = (int)((kSmemBudgetR - fixed) / stage);

@@ -21,17 +21,19 @@
 // bias term is one m16n8k8 per chunk against the group sums Sx split into an
 // fp16 high part and remainder.
 //
-// CTA: 8 consumer warps (warp w owns weight rows n0+32w .. n0+32w+31 for the
-// CTA's whole K range) and two producer warps, which prepare alternate ring
-// stages (one warp alone bounded the pipeline with 8-column fragments).  The
-// producers stream the CTA's 256 rows chunk by chunk (256 codes per row) into
+// CTA: 8 consumer warps (warp w owns two 16-row MMA tiles of weight rows, or
+// one on narrow layers, for the CTA's whole K range: 256- or 128-row CTAs)
+// and two producer warps, which prepare alternate ring stages (one warp alone
+// bounded the pipeline with 8-column fragments).  The producers stream the
+// CTA's rows chunk by chunk (256 codes per row) into
 // the ring: the weight tile with one 2-D TMA copy (64- or 32-byte swizzle, so
 // the quads' 32-bit reads hit 32 distinct banks), the tile's scales and
 // biases once per CTA, all completing on mbarriers.  Weights, scales and
 // biases are requested before the programmatic-dependent-launch wait.
 // K is split over the S CTAs of a thread-block cluster; the partial sums are
-// added in a fixed order through distributed shared memory into rank 0: no
-// global scratch, no atomics, bit-reproducible.  Every mbarrier wait is
+// reduce-scattered through distributed shared memory (st.async completing on
+// the receiving rank's mbarrier) and added in rank order: no global scratch,
+// no atomics, bit-reproducible.  Every mbarrier wait is
 // bounded; on expiry the CTA stops working, drains its copies, passes its
 // remaining barriers, and the expiry is counted for bqd_device_status.
 #include <cudaTypedefs.h>
@@ -175,22 +177,24 @@ __device__ __forceinline__ float h2f_hi(uint32_t w) { return __half2float(__usho
 
 // ---- the kernel --------------------------------------------------------------------
 
-constexpr int kRowsW = 32;              // weight rows per consumer warp: two MMA row tiles
-constexpr int kRowsC = kRowsW * kCons;   // weight rows per CTA
+// TPW MMA row tiles (16 rows each) per consumer warp: 2 (256-row CTAs), or 1
+// (128-row CTAs, twice the CTAs of a narrow layer)
+template <int TPW> constexpr int kRowsWT = 16 * TPW;          // weight rows per consumer warp
+template <int TPW> constexpr int kRowsCT = kRowsWT<TPW> * kCons;  // weight rows per CTA
 
-// One ring stage = one 256-code chunk of the CTA's 256 rows:
-//   weights [256][CB] (TMA, swizzled) | B fragments [8][MP][4] uint4
+// One ring stage = one 256-code chunk of the CTA's rows:
+//   weights [rows][CB] (TMA, swizzled) | B fragments [8][MP][4] uint4
 //   | Cx [4][8] f32 | Sx as fp16 (hi, lo) [8][4]
 // The scales and biases of the CTA's whole K range sit outside the ring, one
-// TMA box each: [256 rows][BX groups] fp16.
+// TMA box each: [rows][BX groups] fp16.
 // a producer's staging of one chunk of x: MP rows of 256 fp16
 template <int MP>
 constexpr int kXRawBytes = MP * kChunkT * 2;
 
-template <int FMT, int GS, bool HAS_BIAS, int MP>
+template <int FMT, int GS, bool HAS_BIAS, int MP, int TPW>
 struct Stage {
     static constexpr int kGPC = kChunkT / GS;
-    static constexpr int kW = kRowsC * TF<FMT, GS>::kChunkBytes;
+    static constexpr int kW = kRowsCT<TPW> * TF<FMT, GS>::kChunkBytes;
     static constexpr int kB = kW;
     static constexpr int kCx = kB + 8 * MP * 4 * 16;
     static constexpr int kSx = kCx + 4 * 8 * 4;
@@ -198,13 +202,16 @@ struct Stage {
 };
 
 
-template <int FMT, int GS, bool HAS_BIAS, int MP>
+template <int FMT, int GS, bool HAS_BIAS, int MP, int TPW>
 __global__ void __launch_bounds__(kThreadsT, 2)
     qmv_tma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap,
                    const __grid_constant__ CUtensorMap bmap, const TmaParams p)
 {
     using F = TF<FMT, GS>;
-    using SL = Stage<FMT, GS, HAS_BIAS, MP>;
+    using SL = Stage<FMT, GS, HAS_BIAS, MP, TPW>;
+    constexpr int kRowsW = kRowsWT<TPW>;
+    constexpr int kRowsC = kRowsCT<TPW>;
+    constexpr int NR = 2 * TPW;  // rows per consumer thread: rb + 8 rr
     constexpr int GPC = SL::kGPC;
     constexpr int NPR = GS / 8;   // fp16x2 registers per (row, group)
     constexpr int MPG = GS / 16;  // MMAs per group
@@ -239,8 +246,8 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t ring_a = smem_addr(smem);
     const uint32_t xraw_a = ring_a + (uint32_t)NST * SL::kBytes;  // per producer [MP][256] fp16
-    const uint32_t sc_a = xraw_a + kProd * kXRawBytes<MP>;          // scales [256][BX] fp16
-    const uint32_t bi_a = sc_a + (uint32_t)(kRowsC * p.BX * 2);     // biases [256][BX] fp16
+    const uint32_t sc_a = xraw_a + kProd * kXRawBytes<MP>;          // scales [rows][BX] fp16
+    const uint32_t bi_a = sc_a + (uint32_t)(kRowsC * p.BX * 2);     // biases [rows][BX] fp16
     float *red = reinterpret_cast<float *>(smem + (size_t)NST * SL::kBytes + kProd * kXRawBytes<MP> +
                                            (size_t)kRowsC * p.BX * 2 * (HAS_BIAS ? 2 : 1));  // [S][RS][8]
     // the scale box starts at a 16-byte aligned group index
@@ -255,7 +262,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         mbar_init(smem_addr(&sc_bar), 1);
         if (S > 1) {
             // rows [rank RS, rank RS + nrow) from all S ranks, ceil(M/2) float pairs a row
-            const int nrow = min(p.RS, kRowsC - rank * p.RS);
+            const int nrow = max(0, min(p.RS, kRowsC - rank * p.RS));
             mbar_init(smem_addr(&red_bar), 1);
             mbar_arrive_expect_tx(smem_addr(&red_bar), (uint32_t)(S * nrow * ((M + 1) / 2) * 8));
         }
@@ -428,9 +435,11 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     }
 
     // ---- consumers: warp w owns rows 32w .. 32w+31 (two MMA row tiles) -------------
-    float acc[2][4];
+    float acc[TPW][4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[0][q] = acc[1][q] = 0.f;
+    for (int tl = 0; tl < TPW; ++tl)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[tl][q] = 0.f;
     const int rb = warp * kRowsW + g;  // rows rb, rb+8 (tile 0), rb+16, rb+24 (tile 1)
     const int jb = t & (GPC - 1);      // bias slot t: group t (gs=64), group t&1 for t < 2 (gs=128)
     uint32_t woff[F::kNW];
@@ -452,9 +461,9 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     for (int it = 0; it < ncl && sc_ok; ++it) {
         if (!wait_bounded(smem_addr(&full_bar[s]), par, p.wait_ns)) break;
         // scales of the four rows for the chunk's groups
-        uint32_t sw[4][GPC / 2];
+        uint32_t sw[NR][GPC / 2];
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
+        for (int rr = 0; rr < NR; ++rr) {
             if constexpr (GPC == 4) {
                 const uint2 a = lds64(sq + rr * R8S);
                 sw[rr][0] = a.x;
@@ -465,9 +474,9 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         }
         // bias term first, straight into the accumulators
         {
-            uint16_t bb[4];
+            uint16_t bb[NR];
 #pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
+            for (int rr = 0; rr < NR; ++rr) {
                 if constexpr (HAS_BIAS) {
                     bb[rr] = lds16(bqb + rr * R8S);
                 } else {
@@ -477,26 +486,28 @@ __global__ void __launch_bounds__(kThreadsT, 2)
                 if (GPC == 2 && t >= 2) bb[rr] = 0;
             }
             const uint32_t sxv = lds32(st_a + sxo);
-            mma_k8(acc[0], dup_half(bb[0]), dup_half(bb[1]), sxv);
-            mma_k8(acc[1], dup_half(bb[2]), dup_half(bb[3]), sxv);
+#pragma unroll
+            for (int tl = 0; tl < TPW; ++tl) mma_k8(acc[tl], dup_half(bb[2 * tl]), dup_half(bb[2 * tl + 1]), sxv);
         }
         const uint32_t bq = st_a + bqo;
 #pragma unroll
         for (int j = 0; j < GPC; ++j) {
-            // this group's words of the four rows, read when needed
-            uint32_t w[4][F::kNW];
+            // this group's words of the thread's rows, read when needed
+            uint32_t w[NR][F::kNW];
 #pragma unroll
-            for (int rr = 0; rr < 4; ++rr)
+            for (int rr = 0; rr < NR; ++rr)
 #pragma unroll
                 for (int v = 0; v < WPG; ++v) {
                     const int idx = j * WPG + v;
                     w[rr][idx] = lds32(st_a + woff[idx] + rr * 8 * CB);
                 }
-            float ag[2][4];
+            float ag[TPW][4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) ag[0][q] = ag[1][q] = 0.f;
+            for (int tl = 0; tl < TPW; ++tl)
 #pragma unroll
-            for (int tl = 0; tl < 2; ++tl) {
+                for (int q = 0; q < 4; ++q) ag[tl][q] = 0.f;
+#pragma unroll
+            for (int tl = 0; tl < TPW; ++tl) {
                 uint32_t A0[NPR], A1[NPR];
                 F::unpack_group(w[2 * tl], j, t, mg, A0);
                 F::unpack_group(w[2 * tl + 1], j, t, mg, A1);
@@ -511,7 +522,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
             const uint2 cxv = lds64(st_a + cxo + (uint32_t)(j * 32));
             const float cx0 = __uint_as_float(cxv.x), cx1 = __uint_as_float(cxv.y);
 #pragma unroll
-            for (int tl = 0; tl < 2; ++tl) {
+            for (int tl = 0; tl < TPW; ++tl) {
                 const float sa = (j & 1) ? h2f_hi(sw[2 * tl][j >> 1]) : h2f_lo(sw[2 * tl][j >> 1]);
                 const float sb = (j & 1) ? h2f_hi(sw[2 * tl + 1][j >> 1]) : h2f_lo(sw[2 * tl + 1][j >> 1]);
                 fma_sub2(acc[tl][0], acc[tl][1], sa, ag[tl][0], ag[tl][1], cx0, cx1);
@@ -533,7 +544,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     // value (tile tl, q) is row rb + 16 tl + 8 (q >> 1), column 2t + (q & 1)
     if (S == 1) {
 #pragma unroll
-        for (int tl = 0; tl < 2; ++tl)
+        for (int tl = 0; tl < TPW; ++tl)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int n = n0 + rb + 16 * tl + 8 * (q >> 1), m = 2 * t + (q & 1);
@@ -552,7 +563,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     if (2 * t < M) {
         const uint32_t rbar = smem_addr(&red_bar);
 #pragma unroll
-        for (int tl = 0; tl < 2; ++tl)
+        for (int tl = 0; tl < TPW; ++tl)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int row = rb + 16 * tl + 8 * h;
@@ -566,7 +577,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     wait_bounded(smem_addr(&red_bar), 0, kDrainWaitNs);
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     const int row0 = rank * RS;
-    const int nrow = min(RS, kRowsC - row0);
+    const int nrow = max(0, min(RS, kRowsC - row0));
     for (int e = tid; e < nrow * M; e += kCons * 32) {
         const int lr = e / M, m = e % M;
         float v = 0.f;
@@ -599,14 +610,14 @@ struct TPlan {
     size_t smem;
 };
 
-template <int FMT, int GS, bool HAS_BIAS, int MP>
+template <int FMT, int GS, bool HAS_BIAS, int MP, int TPW>
 size_t tma_smem(int S, int stages, int RS, int BX)
 {
-    return 1024 + (size_t)stages * Stage<FMT, GS, HAS_BIAS, MP>::kBytes + kProd * kXRawBytes<MP> +
-           (size_t)kRowsC * BX * 2 * (HAS_BIAS ? 2 : 1) + (size_t)S * RS * 8 * 4;
+    return 1024 + (size_t)stages * Stage<FMT, GS, HAS_BIAS, MP, TPW>::kBytes + kProd * kXRawBytes<MP> +
+           (size_t)kRowsCT<TPW> * BX * 2 * (HAS_BIAS ? 2 : 1) + (size_t)S * RS * 8 * 4;
 }
 
-template <int FMT, int GS, bool HAS_BIAS, int MP>
+template <int FMT, int GS, bool HAS_BIAS, int MP, int TPW>
 int cluster_slots_t(int S, size_t smem)
 {
     struct Entry { int dev, S; size_t smem; int slots; };
@@ -618,7 +629,7 @@ int cluster_slots_t(int S, size_t smem)
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < n; ++i)
         if (cache[i].dev == dev && cache[i].S == S && cache[i].smem == smem) return cache[i].slots;
-    auto kern = qmv_tma_kernel<FMT, GS, HAS_BIAS, MP>;
+    auto kern = qmv_tma_kernel<FMT, GS, HAS_BIAS, MP, TPW>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudgetT);
     cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaLaunchConfig_t cfg = {};
@@ -642,32 +653,36 @@ int cluster_slots_t(int S, size_t smem)
 }
 
 // P passes of x rows run side by side in one launch (grid rows)
-template <int FMT, int GS, bool HAS_BIAS, int MP>
+template <int FMT, int GS, bool HAS_BIAS, int MP, int TPW>
 bool plan_t(int N, int chunks, int P, TPlan &best)
 {
     constexpr int GPC = kChunkT / GS;
+    constexpr int kRowsC = kRowsCT<TPW>;
     const int R = (N + kRowsC - 1) / kRowsC;
     const int sms = sm_count();
-    const size_t stage = Stage<FMT, GS, HAS_BIAS, MP>::kBytes;
+    const size_t stage = Stage<FMT, GS, HAS_BIAS, MP, TPW>::kBytes;
     double best_cost = 1e30;
     bool found = false;
     for (int S = 1; S <= kMaxSplitT && S <= chunks; ++S) {
         const int Cs = (chunks + S - 1) / S;
         if ((S - 1) * Cs >= chunks) continue;
         const int RS = (kRowsC + S - 1) / S;
+        // every rank owns rows of the reduction (128 rows over 14 ranks would
+        // leave the last one none)
+        if ((S - 1) * RS >= kRowsC) continue;
         // scale box: the rank's groups from the 16-byte aligned group below its first
         int maxoff = 0;
         for (int r = 0; r < S; ++r) maxoff = std::max(maxoff, (r * Cs * GPC) & 7);
         const int BX = (Cs * GPC + maxoff + 7) / 8 * 8;
         if (BX > 256) continue;
-        const size_t fixed = tma_smem<FMT, GS, HAS_BIAS, MP>(S, 0, RS, BX);
+        const size_t fixed = tma_smem<FMT, GS, HAS_BIAS, MP, TPW>(S, 0, RS, BX);
         if (fixed + stage > kSmemBudgetT) continue;
         int st = (int)((kSmemBudgetT - fixed) / stage);
         st = st > kMaxStagesT ? kMaxStagesT : st;
         st = st > Cs ? Cs : st;
         if (st < 2 && Cs > 1) continue;
-        const size_t sm = tma_smem<FMT, GS, HAS_BIAS, MP>(S, st, RS, BX);
-        const int slots = S == 1 ? 2 * sms : cluster_slots_t<FMT, GS, HAS_BIAS, MP>(S, sm);
+        const size_t sm = tma_smem<FMT, GS, HAS_BIAS, MP, TPW>(S, st, RS, BX);
+        const int slots = S == 1 ? 2 * sms : cluster_slots_t<FMT, GS, HAS_BIAS, MP, TPW>(S, sm);
         if (slots <= 0) continue;
         const int waves = (R * P + slots - 1) / slots;
         // time ~ waves x (chunks per CTA + first-stage latency and reduction, ~2 chunks)
@@ -681,26 +696,26 @@ bool plan_t(int N, int chunks, int P, TPlan &best)
     return found;
 }
 
-// 2-D tensor map of a row-major [rows][cols] fp16 array, box {box_cols, 256}
-bool encode_f16(CUtensorMap &map, const __half *base, int64_t cols, int64_t rows, int box_cols)
+// 2-D tensor map of a row-major [rows][cols] fp16 array, box {box_cols, box_rows}
+bool encode_f16(CUtensorMap &map, const __half *base, int64_t cols, int64_t rows, int box_cols, int box_rows)
 {
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)kRowsC};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int FMT, int GS, bool HAS_BIAS, int MP>
+template <int FMT, int GS, bool HAS_BIAS, int MP, int TPW>
 int launch_t(const TmaParams &p0, const CUtensorMap &map, int chunks, cudaStream_t s)
 {
     TPlan pl;
     const int P = (p0.M + 7) / 8;
-    if (!plan_t<FMT, GS, HAS_BIAS, MP>(p0.N, chunks, P, pl)) return BQD_ERR_UNSUPPORTED;
+    if (!plan_t<FMT, GS, HAS_BIAS, MP, TPW>(p0.N, chunks, P, pl)) return BQD_ERR_UNSUPPORTED;
     TmaParams p = p0;
     p.S = pl.S;
     p.Cs = pl.Cs;
@@ -708,13 +723,14 @@ int launch_t(const TmaParams &p0, const CUtensorMap &map, int chunks, cudaStream
     p.RS = pl.RS;
     p.BX = pl.BX;
     CUtensorMap smap, bmap;
-    if (!encode_f16(smap, p.scales, p.G, p.N, pl.BX)) return BQD_ERR_CUDA;
+    if (!encode_f16(smap, p.scales, p.G, p.N, pl.BX, kRowsCT<TPW>)) return BQD_ERR_CUDA;
     bmap = smap;
-    if (HAS_BIAS && !encode_f16(bmap, p.biases, p.G, p.N, pl.BX)) return BQD_ERR_CUDA;
+    if (HAS_BIAS && !encode_f16(bmap, p.biases, p.G, p.N, pl.BX, kRowsCT<TPW>)) return BQD_ERR_CUDA;
     if (opt_debug_plan())
-        fprintf(stderr, "bqd tma plan: N=%d K=%d M=%d gs=%d -> S=%d Cs=%d stages=%d R=%d BX=%d grid=%dx%d smem=%zu\n",
-                p.N, p.K, p.M, GS, pl.S, pl.Cs, pl.stages, pl.R, pl.BX, pl.R * pl.S, P, pl.smem);
-    auto kern = qmv_tma_kernel<FMT, GS, HAS_BIAS, MP>;
+        fprintf(stderr,
+                "bqd tma plan: N=%d K=%d M=%d gs=%d -> rows=%d S=%d Cs=%d stages=%d R=%d BX=%d grid=%dx%d smem=%zu\n",
+                p.N, p.K, p.M, GS, kRowsCT<TPW>, pl.S, pl.Cs, pl.stages, pl.R, pl.BX, pl.R * pl.S, P, pl.smem);
+    auto kern = qmv_tma_kernel<FMT, GS, HAS_BIAS, MP, TPW>;
     static int configured_dev[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -746,12 +762,22 @@ int launch_t(const TmaParams &p0, const CUtensorMap &map, int chunks, cudaStream
     return cudaLaunchKernelEx(&cfg, kern, map, smap, bmap, p) == cudaSuccess ? BQD_OK : BQD_ERR_CUDA;
 }
 
-template <int FMT, int GS>
+template <int FMT, int GS, int TPW>
 int launch_fmt_gs(const TmaParams &p, const CUtensorMap &map, int chunks, bool has_bias, int MP, cudaStream_t s)
 {
     if (MP == 4)
-        return has_bias ? launch_t<FMT, GS, true, 4>(p, map, chunks, s) : launch_t<FMT, GS, false, 4>(p, map, chunks, s);
-    return has_bias ? launch_t<FMT, GS, true, 8>(p, map, chunks, s) : launch_t<FMT, GS, false, 8>(p, map, chunks, s);
+        return has_bias ? launch_t<FMT, GS, true, 4, TPW>(p, map, chunks, s)
+                        : launch_t<FMT, GS, false, 4, TPW>(p, map, chunks, s);
+    return has_bias ? launch_t<FMT, GS, true, 8, TPW>(p, map, chunks, s)
+                    : launch_t<FMT, GS, false, 8, TPW>(p, map, chunks, s);
+}
+
+template <int FMT, int GS>
+int launch_fmt_gs(const TmaParams &p, const CUtensorMap &map, int chunks, bool has_bias, int MP, int tpw,
+                  cudaStream_t s)
+{
+    return tpw == 1 ? launch_fmt_gs<FMT, GS, 1>(p, map, chunks, has_bias, MP, s)
+                    : launch_fmt_gs<FMT, GS, 2>(p, map, chunks, has_bias, MP, s);
 }
 
 }  // namespace
@@ -779,10 +805,14 @@ int launch_qmv_tma(const QmvArgs &a, cudaStream_t s)
     if (!enc) return BQD_ERR_UNSUPPORTED;
 
     const bool b64 = a.fmt == BQD_FMT_AFFINE2;
+    // narrow layers (at most eight 256-row blocks): 128-row CTAs, one 16-row
+    // tile per consumer warp, so that twice the CTAs share the work and a
+    // warp's work per stage halves
+    const int tpw = a.N <= 2048 ? 1 : 2;
     CUtensorMap map;
     cuuint64_t dims[2] = {(cuuint64_t)a.row_bytes, (cuuint64_t)a.N};
     cuuint64_t strides[1] = {(cuuint64_t)a.row_bytes};
-    cuuint32_t box[2] = {b64 ? 64u : 32u, (cuuint32_t)kRowsC};
+    cuuint32_t box[2] = {b64 ? 64u : 32u, (cuuint32_t)(16 * tpw * kCons)};
     cuuint32_t estr[2] = {1, 1};
     CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.w), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, b64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
@@ -806,10 +836,10 @@ int launch_qmv_tma(const QmvArgs &a, cudaStream_t s)
     p.x = a.x;
     p.out = a.out;
     if (b64)
-        return a.gs == 64 ? launch_fmt_gs<BQD_FMT_AFFINE2, 64>(p, map, p.chunks, hb, MP, s)
-                          : launch_fmt_gs<BQD_FMT_AFFINE2, 128>(p, map, p.chunks, hb, MP, s);
-    return a.gs == 64 ? launch_fmt_gs<BQD_FMT_AFFINE1, 64>(p, map, p.chunks, hb, MP, s)
-                      : launch_fmt_gs<BQD_FMT_AFFINE1, 128>(p, map, p.chunks, hb, MP, s);
+        return a.gs == 64 ? launch_fmt_gs<BQD_FMT_AFFINE2, 64>(p, map, p.chunks, hb, MP, tpw, s)
+                          : launch_fmt_gs<BQD_FMT_AFFINE2, 128>(p, map, p.chunks, hb, MP, tpw, s);
+    return a.gs == 64 ? launch_fmt_gs<BQD_FMT_AFFINE1, 64>(p, map, p.chunks, hb, MP, tpw, s)
+                      : launch_fmt_gs<BQD_FMT_AFFINE1, 128>(p, map, p.chunks, hb, MP, tpw, s);
 }
 
 }  // namespace bqd

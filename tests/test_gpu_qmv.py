@@ -77,11 +77,13 @@ def test_tensor_core_paths_forced(kernel, fmt, gs, sym):
 
 
 # TMA-ring kernel: its envelope is K a multiple of 256 with K/gs a multiple of
-# 8 (16-byte scale rows); shapes span row blocks of 256 with ragged tails,
-# split-K clusters of many sizes (portable and not), M up to 8 in one pass and
-# passes of 8 rows (grid rows of one launch) beyond (every M from 9 to 16,
-# and 27 and 33), the last one ragged
-TMA_SHAPES = [(1, 1, 1024), (2, 127, 1024), (3, 256, 2048), (4, 257, 3072), (5, 383, 4096), (7, 1024, 5120),
+# 8 (16-byte scale rows); shapes span row blocks of 128 (N <= 2048) and 256
+# (larger N) with ragged tails, both sides of N = 2048, split-K clusters of
+# many sizes (portable and not; 300 x 17408 would take 14 ranks, which leave
+# one of them no rows of a 128-row block, so the planner skips that split), M
+# up to 8 in one pass and passes of 8 rows (grid rows of one launch) beyond
+# (every M from 9 to 16, and 27 and 33), the last one ragged
+TMA_SHAPES = [(1, 2048, 2048), (3, 2100, 1024), (1, 1, 1024), (2, 127, 1024), (3, 256, 2048), (4, 257, 3072), (5, 383, 4096), (7, 1024, 5120),
               (8, 2000, 1024), (9, 200, 2048), (16, 130, 1024), (1, 5120, 17408), (5, 300, 17408), (2, 4096, 6144),
               (27, 300, 2048), (6, 70, 1024), (10, 513, 2048), (11, 64, 5120), (12, 300, 3072), (13, 257, 1024),
               (14, 1000, 2048), (15, 33, 4096), (33, 129, 1024)]
@@ -101,8 +103,9 @@ def test_tma_kernel_shapes(fmt, gs, sym):
 # layers) and 256-row blocks (4353 x 5120, 4100 x 17408, 5120 x 17408), split-K
 # clusters, the column split (M <= 2) and the scaled path (M >= 3), passes of
 # at most 8 x rows (grid rows of one launch; M = 12, 16, 23 take several, the
-# last one ragged)
-T5R_SHAPES = [(1, 1, 1024), (2, 127, 1024), (2, 255, 1024), (3, 129, 2048), (3, 257, 2048), (4, 300, 3072),
+# last one ragged); K = 28672 (28 chunks) is where 14 ranks would leave one
+# of them no rows of a 128-row block: the planner skips that split
+T5R_SHAPES = [(1, 300, 28672), (4, 200, 28672), (1, 1, 1024), (2, 127, 1024), (2, 255, 1024), (3, 129, 2048), (3, 257, 2048), (4, 300, 3072),
               (4, 513, 1024), (5, 1000, 5120), (6, 383, 4096), (6, 511, 3072), (7, 260, 2048), (12, 64, 1024),
               (16, 130, 2048), (1, 5120, 17408), (5, 200, 17408), (23, 129, 2048), (1, 4353, 5120),
               (2, 4100, 17408), (3, 4353, 5120), (8, 4100, 17408)]
