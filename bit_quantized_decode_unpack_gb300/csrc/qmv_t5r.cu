@@ -38,13 +38,15 @@
 //    groups per chunk, against the group sums of x split into an fp16 high
 //    part and remainder.
 //
-// CTA: NW consumer warps (warp w owns weight rows n0+16w .. +15) and one
-// producer warp; NW = 8 (128 rows, two CTAs per SM) for passes of up to five
-// x rows, 16 (256 rows, one CTA per SM) for larger passes.  Per ring stage (one 1024-code chunk of
-// the CTA's rows) the producer issues the 2-D TMA copies of the weights
-// [rows][208 B], the scales and the biases, then builds the B fragments from
-// the chunk of x (TMA into a double buffer, one chunk ahead; each pass of the
-// warp gathers from one x row) and the sums above.  Weights, scales and
+// CTA: NW consumer warps (warp w owns weight rows n0+16w .. +15) and two
+// producer warps, which prepare alternate chunks (one alone could not keep up
+// with the consumers from two x rows on); NW = 8 (128 rows, two CTAs per SM)
+// for passes of up to five x rows, 16 (256 rows, one CTA per SM) for larger
+// passes.  Per ring stage (one 1024-code chunk of the CTA's rows) a producer
+// issues the 2-D TMA copies of the weights [rows][208 B], the scales and the
+// biases, then builds the B fragments from the chunk of x (TMA into its own
+// buffer, requested once its previous chunk's fragments are built; each pass
+// of the warp gathers from one x row) and the sums above.  Weights, scales and
 // biases are requested before the programmatic-dependent-launch wait.  K is
 // split over the S CTAs of a cluster.  The partial sums are reduce-scattered
 // through distributed shared memory, each rank adding its slice of rows in
@@ -77,11 +79,13 @@ constexpr int kMaxMR = 8;                      // x rows per pass (the MMA's N)
 constexpr int kMaxStagesR = 4;
 constexpr int kMaxSplitR = 16;
 
-// CTA shape: NW consumer warps of 16 weight rows each plus one producer warp:
-// NW = 8 (128 rows, two CTAs per SM) or NW = 16 (256 rows, one CTA per SM).
+// CTA shape: NW consumer warps of 16 weight rows each plus two producer warps
+// (alternate chunks): NW = 8 (128 rows, two CTAs per SM) or NW = 16 (256 rows,
+// one CTA per SM).
+constexpr int kProdR = 2;
 template <int NW>
 struct Cta {
-    static constexpr int kThreads = (NW + 1) * 32;
+    static constexpr int kThreads = (NW + kProdR) * 32;
     static constexpr int kRows = 16 * NW;
     static constexpr int kPerSM = NW == 16 ? 1 : 2;
     static constexpr size_t kSmemBudget = NW == 16 ? 224 * 1024 : 110 * 1024;  // dynamic (static ~3 KB)
@@ -370,6 +374,7 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
     __shared__ __align__(8) uint64_t full_bar[kMaxStagesR], empty_bar[kMaxStagesR], x_bar[2];
     __shared__ __align__(8) uint64_t red_bar;  // split K: this rank's rows of every rank's partials have landed
     __shared__ __align__(16) uint16_t koff[kPairsR * 4 * 8];  // (pair, slot, half) -> staging offset
+    __shared__ int last_it[kMaxStagesR];  // iteration whose weights a stage received last (-1: none)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -388,7 +393,7 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t ring_a = smem_addr(smem);
-    const uint32_t xraw_a = ring_a + (uint32_t)NST * STB;  // 2 x [M][1024] fp16, producer only
+    const uint32_t xraw_a = ring_a + (uint32_t)NST * STB;  // 2 x [M][1024] fp16: producer pw's buffer is pw
     const uint32_t XB = (uint32_t)(M * kCodesR * 2);
     float *red = reinterpret_cast<float *>(smem + (size_t)NST * STB + 2 * (size_t)XB);  // [S][RS][8]
 
@@ -427,16 +432,30 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
         for (int i = tid; i < 4 * NST; i += kThreadsR)
             sts128(ring_a + (uint32_t)(i >> 2) * STB + (uint32_t)(SL::zero_off(M) + (i & 3) * 16), make_uint4(0, 0, 0, 0));
     }
+    // B gather table: entry (pair ip, slot, q) is half q & 1 of item 2i + ((q >> 1) & 1)
+    // of MMA 2ip + (q >> 2) = period pp, MMA i; staging layout [box k/256][x row][256]
+    for (int e = tid; e < kPairsR * 4 * 8; e += kThreadsR) {
+        const int q = e & 7, slot = (e >> 3) & 3, ip = e >> 5;
+        const int i0 = 2 * ip + (q >> 2);
+        const int pp = i0 / MPG, i = i0 % MPG;
+        const int u = 2 * i + ((q >> 1) & 1);
+        const int code = (q & 1) ? c_t5.hi[GS == 128][u] : c_t5.lo[GS == 128][u];
+        const int kc = (NG * slot + pp) * GS + code;
+        koff[e] = (uint16_t)((kc >> 8) * M * 512 + (kc & 255) * 2);
+    }
+    if (tid < kMaxStagesR) last_it[tid] = -1;
     __syncthreads();
     // split phase: every CTA of the cluster has started, with its reduction
     // barrier set up, before any distributed-shared-memory store (the matching
     // wait is before them)
     if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
-    if (warp == NW) {
-        // ---- producer ----------------------------------------------------------------
+    if (warp >= NW) {
+        // ---- producers: pw prepares chunks pw, pw + 2, ... from x buffer pw -----------
+        const int pw = warp - NW;
         auto issue = [&](int it, int s) {
             if (lane == 0) {
+                last_it[s] = it;
                 const uint32_t bar = smem_addr(&full_bar[s]);
                 const uint32_t st = ring_a + (uint32_t)s * STB;
                 mbar_arrive_expect_tx(bar, (uint32_t)(SL::kW + SL::kS * (HAS_BIAS ? 2 : 1)));
@@ -446,7 +465,7 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
                 if (HAS_BIAS) tma_2d(st + SL::kBias, &bmap, c * GPC, n0, bar);
             }
         };
-        // x of chunk `it` (four 256-code boxes of M rows) into staging buffer it & 1
+        // x of chunk `it` (four 256-code boxes of M rows) into staging buffer it & 1 (= pw)
         auto issue_x = [&](int it) {
             if (lane == 0) {
                 const uint32_t bar = smem_addr(&x_bar[it & 1]);
@@ -459,17 +478,10 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
             }
         };
         const int pre = min(NST, ncl);
-        for (int it = 0; it < pre; ++it) issue(it, it);
-        // B gather table: entry (pair ip, slot, q) is half q & 1 of item 2i + ((q >> 1) & 1)
-        // of MMA 2ip + (q >> 2) = period pp, MMA i; staging layout [box k/256][x row][256]
-        for (int e = lane; e < kPairsR * 4 * 8; e += 32) {
-            const int q = e & 7, slot = (e >> 3) & 3, ip = e >> 5;
-            const int i0 = 2 * ip + (q >> 2);
-            const int pp = i0 / MPG, i = i0 % MPG;
-            const int u = 2 * i + ((q >> 1) & 1);
-            const int code = (q & 1) ? c_t5.hi[GS == 128][u] : c_t5.lo[GS == 128][u];
-            const int kc = (NG * slot + pp) * GS + code;
-            koff[e] = (uint16_t)((kc >> 8) * M * 512 + (kc & 255) * 2);
+        int issued_end = pw;  // this producer's iterations below issued_end have their weights requested
+        for (int it = pw; it < pre; it += kProdR) {
+            issue(it, it);
+            issued_end = it + kProdR;
         }
         // indicator A rows of the group sums: row r is 1 on the k-slots of
         // group r (thread t's slots of period P hold group NG t + P)
@@ -486,27 +498,29 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
         aofs[1] = g == 0 ? 0x3C003C00u : (g == 1 ? (0x64006400u ^ p.zero) : 0u);
         __syncwarp();
         pdl_wait();
-        if (ncl > 0) issue_x(0);
-        int s = 0, done = 0, issued_w = pre;
-        uint32_t par = 0;
-        for (int it = 0; it < ncl; ++it) {
+        int x_next = ncl;  // the chunk whose x copy is in flight and not yet awaited (ncl: none)
+        if (pw < ncl) {
+            issue_x(pw);
+            x_next = pw;
+        }
+        int done = pw;  // this producer's iterations below done are prepared
+        for (int it = pw; it < ncl; it += kProdR) {
+            const int s = it % NST;
+            const uint32_t par = (uint32_t)(it / NST) & 1u;
             const uint32_t st = ring_a + (uint32_t)s * STB;
             if (it >= NST) {
                 bool ok = lane == 0 ? wait_bounded_r(smem_addr(&empty_bar[s]), par ^ 1u, p.wait_ns) : true;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
                 issue(it, s);
-                issued_w = it + 1;
+                issued_end = it + kProdR;
             }
             {
                 bool ok = lane == 0 ? wait_bounded_r(smem_addr(&x_bar[it & 1]), (it >> 1) & 1, p.wait_ns) : true;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
+                x_next = ncl;
             }
-            // the other buffer was last read while preparing chunk it-1 (finished,
-            // see the __syncwarp below): order those reads before the next copy
-            fence_proxy_async_smem();
-            if (it + 1 < ncl) issue_x(it + 1);
             const uint32_t xb = xraw_a + (uint32_t)(it & 1) * XB;
             // B fragments: entry (ip, x row m, slot) at kB + ((ip M + m) 4 + slot) 16.
             // Each pass of the warp gathers from one x row (rows are 512 bytes
@@ -530,7 +544,15 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
                 sts128(st + SL::kB + (uint32_t)(e * 16), make_uint4(__byte_perm(h[0], h[1], 0x5410), __byte_perm(h[2], h[3], 0x5410),
                                                                    __byte_perm(h[4], h[5], 0x5410), __byte_perm(h[6], h[7], 0x5410)));
             }
+            // the buffer's reads are done: order them before the copy of this
+            // producer's next chunk into it
             __syncwarp();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (it + kProdR < ncl) {
+                issue_x(it + kProdR);
+                x_next = it + kProdR;
+            }
             if constexpr (COL) {
                 // Sx (row 0) and Cx (row 1) of every (period, slot, x row): the
                 // consumers' MMA sequence (two chains per period) over a constant A
@@ -587,23 +609,24 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
                     }
                 }
             }
-            __syncwarp();  // the staging area is rewritten by the next chunk
+            __syncwarp();
             mbar_arrive_r(smem_addr(&full_bar[s]));
-            done = it + 1;
-            if (++s == NST) {
-                s = 0;
-                par ^= 1u;
-            }
+            done = it + kProdR;
         }
-        // every copy this CTA issued has landed before anyone leaves: stages whose
-        // weights were requested but that were never prepared (a wait expired)
-        // get their missing arrivals, then the last stages are awaited; the x
-        // copy of chunk `done` is in flight whenever the loop stopped early
-        for (int it = done; it < issued_w; ++it) mbar_arrive_r(smem_addr(&full_bar[it % NST]));
+        // every copy this CTA issued has landed before anyone leaves: this
+        // producer's stages whose weights were requested but that were never
+        // prepared (a wait expired) get their missing arrivals; once both
+        // producers have stopped issuing, each awaits the stages it filled last
+        // and its x copy still in flight
+        for (int it = done; it < issued_end; it += kProdR) mbar_arrive_r(smem_addr(&full_bar[it % NST]));
+        asm volatile("bar.sync 1, %0;" ::"n"(kProdR * 32) : "memory");
         if (lane == 0) {
-            for (int it = max(0, issued_w - NST); it < issued_w; ++it)
-                wait_bounded_r(smem_addr(&full_bar[it % NST]), (it / NST) & 1, kDrainWaitNs);
-            if (done < ncl) wait_bounded_r(smem_addr(&x_bar[done & 1]), (done >> 1) & 1, kDrainWaitNs);
+            for (int s = 0; s < NST; ++s) {
+                const int li = last_it[s];
+                if (li >= 0 && li % kProdR == pw)
+                    wait_bounded_r(smem_addr(&full_bar[s]), (uint32_t)(li / NST) & 1u, kDrainWaitNs);
+            }
+            if (x_next < ncl) wait_bounded_r(smem_addr(&x_bar[x_next & 1]), (x_next >> 1) & 1, kDrainWaitNs);
         }
         __syncwarp();
         if (S > 1) {
