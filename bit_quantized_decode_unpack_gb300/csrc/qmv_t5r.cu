@@ -44,9 +44,10 @@
 // for passes of up to five x rows, 16 (256 rows, one CTA per SM) for larger
 // passes.  Per ring stage (one 1024-code chunk of the CTA's rows) a producer
 // issues the 2-D TMA copies of the weights [rows][208 B], the scales and the
-// biases, then builds the B fragments from the chunk of x (TMA into its own
-// buffer, requested once its previous chunk's fragments are built; each pass
-// of the warp gathers from one x row) and the sums above.  Weights, scales and
+// biases, then builds the B fragments from the chunk of x (16-byte copies
+// through the load/store path into its own buffer, requested once its previous
+// chunk's fragments are built; each pass of the warp gathers from one x row)
+// and the sums above.  Weights, scales and
 // biases are requested before the programmatic-dependent-launch wait.  K is
 // split over the S CTAs of a cluster.  The partial sums are reduce-scattered
 // through distributed shared memory, each rank adding its slice of rows in
@@ -221,6 +222,15 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int
         : "memory");
 }
 
+// 16 bytes global -> shared through the load/store path (src_bytes 0: zeros);
+// a thread's copies complete at its cp.async.wait_all
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ void sts128(uint32_t a, uint4 v)
 {
     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
@@ -361,7 +371,7 @@ __device__ __forceinline__ uint32_t scale_item(uint32_t a, uint32_t s2, uint32_t
 template <int GS, bool HAS_BIAS, bool COL, int NW>
 __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
     qmv_t5r_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap,
-                   const __grid_constant__ CUtensorMap bmap, const __grid_constant__ CUtensorMap xmap, const T5RParams p)
+                   const __grid_constant__ CUtensorMap bmap, const T5RParams p)
 {
     using Ge = T5G<GS>;
     using SL = Stage5<GS, HAS_BIAS, COL, NW>;
@@ -371,7 +381,7 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
     constexpr int GPC = Ge::GPC;
     constexpr int MPG = Ge::MPG;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[kMaxStagesR], empty_bar[kMaxStagesR], x_bar[2];
+    __shared__ __align__(8) uint64_t full_bar[kMaxStagesR], empty_bar[kMaxStagesR];
     __shared__ __align__(8) uint64_t red_bar;  // split K: this rank's rows of every rank's partials have landed
     __shared__ __align__(16) uint16_t koff[kPairsR * 4 * 8];  // (pair, slot, half) -> staging offset
     __shared__ int last_it[kMaxStagesR];  // iteration whose weights a stage received last (-1: none)
@@ -417,8 +427,6 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
             mbar_init(smem_addr(&full_bar[s]), 33);  // producer lane 0 (expect_tx) + 32 once x is prepared
             mbar_init(smem_addr(&empty_bar[s]), NW * 32);
         }
-        mbar_init(smem_addr(&x_bar[0]), 1);
-        mbar_init(smem_addr(&x_bar[1]), 1);
         if (S > 1) {
             // rows [rank RS, rank RS + nrow) from all S ranks: M floats a row
             // (column split), else ceil(M/2) float pairs
@@ -465,17 +473,22 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
                 if (HAS_BIAS) tma_2d(st + SL::kBias, &bmap, c * GPC, n0, bar);
             }
         };
-        // x of chunk `it` (four 256-code boxes of M rows) into staging buffer it & 1 (= pw)
+        // x of chunk `it` into staging buffer it & 1 (= pw), laid out [256-code box
+        // j][x row m][256], by 16-byte copies of the warp's lanes through the
+        // load/store path (a TMA copy would queue behind the weight copies);
+        // a pass's rows past the call's M read as zeros
         auto issue_x = [&](int it) {
-            if (lane == 0) {
-                const uint32_t bar = smem_addr(&x_bar[it & 1]);
-                mbar_arrive_expect_tx(bar, XB);
-                const int k0 = (c_lo + it) * kCodesR;
+            const uint32_t xb = xraw_a + (uint32_t)(it & 1) * XB;
+            const int k0 = (c_lo + it) * kCodesR + 8 * lane;
+            for (int m = 0; m < M; ++m) {
+                const int row = M * (int)blockIdx.y + m;
+                const bool in = row < p.Mtot;
+                const __half *src = p.x + (size_t)(in ? row : 0) * p.K + k0;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    tma_2d(xraw_a + (uint32_t)(it & 1) * XB + (uint32_t)(j * 512 * M), &xmap, k0 + 256 * j,
-                           M * (int)blockIdx.y, bar);
+                    cp_async16(xb + (uint32_t)((j * M + m) * 512 + 16 * lane), src + 256 * j, in ? 16u : 0u);
             }
+            cp_async_commit();
         };
         const int pre = min(NST, ncl);
         int issued_end = pw;  // this producer's iterations below issued_end have their weights requested
@@ -498,11 +511,7 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
         aofs[1] = g == 0 ? 0x3C003C00u : (g == 1 ? (0x64006400u ^ p.zero) : 0u);
         __syncwarp();
         pdl_wait();
-        int x_next = ncl;  // the chunk whose x copy is in flight and not yet awaited (ncl: none)
-        if (pw < ncl) {
-            issue_x(pw);
-            x_next = pw;
-        }
+        if (pw < ncl) issue_x(pw);
         int done = pw;  // this producer's iterations below done are prepared
         for (int it = pw; it < ncl; it += kProdR) {
             const int s = it % NST;
@@ -515,12 +524,9 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
                 issue(it, s);
                 issued_end = it + kProdR;
             }
-            {
-                bool ok = lane == 0 ? wait_bounded_r(smem_addr(&x_bar[it & 1]), (it >> 1) & 1, p.wait_ns) : true;
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                x_next = ncl;
-            }
+            // x of chunk it: each lane's copies, then every lane's
+            cp_async_wait_all();
+            __syncwarp();
             const uint32_t xb = xraw_a + (uint32_t)(it & 1) * XB;
             // B fragments: entry (ip, x row m, slot) at kB + ((ip M + m) 4 + slot) 16.
             // Each pass of the warp gathers from one x row (rows are 512 bytes
@@ -544,15 +550,10 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
                 sts128(st + SL::kB + (uint32_t)(e * 16), make_uint4(__byte_perm(h[0], h[1], 0x5410), __byte_perm(h[2], h[3], 0x5410),
                                                                    __byte_perm(h[4], h[5], 0x5410), __byte_perm(h[6], h[7], 0x5410)));
             }
-            // the buffer's reads are done: order them before the copy of this
-            // producer's next chunk into it
+            // every lane's reads of the buffer are done before any lane's copy
+            // of this producer's next chunk rewrites it
             __syncwarp();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (it + kProdR < ncl) {
-                issue_x(it + kProdR);
-                x_next = it + kProdR;
-            }
+            if (it + kProdR < ncl) issue_x(it + kProdR);
             if constexpr (COL) {
                 // Sx (row 0) and Cx (row 1) of every (period, slot, x row): the
                 // consumers' MMA sequence (two chains per period) over a constant A
@@ -617,7 +618,7 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
         // producer's stages whose weights were requested but that were never
         // prepared (a wait expired) get their missing arrivals; once both
         // producers have stopped issuing, each awaits the stages it filled last
-        // and its x copy still in flight
+        // (and each lane its x copies still in flight)
         for (int it = done; it < issued_end; it += kProdR) mbar_arrive_r(smem_addr(&full_bar[it % NST]));
         asm volatile("bar.sync 1, %0;" ::"n"(kProdR * 32) : "memory");
         if (lane == 0) {
@@ -626,8 +627,8 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
                 if (li >= 0 && li % kProdR == pw)
                     wait_bounded_r(smem_addr(&full_bar[s]), (uint32_t)(li / NST) & 1u, kDrainWaitNs);
             }
-            if (x_next < ncl) wait_bounded_r(smem_addr(&x_bar[x_next & 1]), (x_next >> 1) & 1, kDrainWaitNs);
         }
+        cp_async_wait_all();
         __syncwarp();
         if (S > 1) {
             asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
@@ -1019,10 +1020,6 @@ int launch_r(const T5RParams &p0, int64_t row_bytes, cudaStream_t s)
     bmap = smap;
     if (HAS_BIAS && !encode_2d(bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.biases, p.G, p.N, (int64_t)p.G * 2, GPC, Cta<NW>::kRows))
         return BQD_ERR_CUDA;
-    // x: [Mtot][K] fp16, box {256 codes, M rows}; a pass's rows past Mtot read as zeros
-    CUtensorMap xmap;
-    if (!encode_2d(xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.x, p.K, p.Mtot, (int64_t)p.K * 2, 256, p.M))
-        return BQD_ERR_CUDA;
     if (opt_debug_plan())
         fprintf(stderr, "bqd t5r plan: N=%d K=%d M=%d (%d per pass) gs=%d col=%d rows=%d -> S=%d Cs=%d stages=%d R=%d grid=%dx%d smem=%zu\n",
                 p.N, p.K, p.Mtot, p.M, GS, (int)COL, Cta<NW>::kRows, pl.S, pl.Cs, pl.stages, pl.R, pl.R * pl.S, P, pl.smem);
@@ -1055,7 +1052,7 @@ int launch_r(const T5RParams &p0, int64_t row_bytes, cudaStream_t s)
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, wmap, smap, bmap, xmap, p) == cudaSuccess ? BQD_OK : BQD_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, kern, wmap, smap, bmap, p) == cudaSuccess ? BQD_OK : BQD_ERR_CUDA;
 }
 
 }  // namespace
