@@ -10,21 +10,24 @@
 //   Y[m, n] = sum_k X[m, k] * W[n, k],  W[n, k] = fp16(fp16(s[n,g] * q[n,k]) + b[n,g])
 //   (sym: b = fp16(-ratio * s); t5 with the default ratio 1 gives W = s*(t-1))
 //
-// One CTA owns 128 weight rows x BX activation rows (BX = 32, 64, 128 or 256)
-// and a range of K groups.  When the (weight, activation) tiles are too few to
-// fill the GPU, the K range is split over the CTAs of a cluster and the
-// partial tiles are reduced through distributed shared memory (no global
+// One CTA owns 128 weight rows x BX activation rows (BX = 32, 64, 128 or 256;
+// on wide layers with M > 256 two blocks of 256, K steps of 64 codes) and a
+// range of K groups.  When the (weight, activation) tiles are too few to fill
+// the GPU, the K range is split over the CTAs of a cluster: each rank owns a
+// slice of the 32-column blocks, receives the other ranks' partials of it
+// through distributed shared memory and adds them in rank order (no global
 // scratch).
 //
 // Roles (320 threads):
 //   warps 0-7  decode: thread (r, h) = (tid % 128, warp / 4) decodes half h of
-//              weight row n0+r's group per K step (one group of gs codes),
-//              forms the fp16 weights and stores them into the stage's A tile
-//              in the tcgen05 K-major 128-byte-swizzled layout.
-//              t5: codes [0, gs/2) or [gs/2, gs), both starting on an even
-//              byte, so byte pairs decode as a unit: the group's t5 bytes go
-//              through a shared byte->trits table, then a magic-exponent LOP3
-//              + HFMA2 give s*t exactly, then + b.
+//              weight row n0+r's codes per K step (a group of gs codes, or
+//              half of a 128-code group in the two-block mode), forms the fp16
+//              weights and stores them into the stage's A tile in the tcgen05
+//              K-major 128-byte-swizzled layout.
+//              t5: a half starts inside a byte (byte 0, 6, 12 or 18 of a group;
+//              byte pairs decode as a unit and the half's codes are picked out
+//              of them): the bytes go through a shared byte->trits table, then
+//              a magic-exponent LOP3 + HFMA2 give s*t exactly, then + b.
 //              1/2-bit: the half group is one aligned 4-, 8- or 16-byte load;
 //              a byte is duplicated into both 16-bit halves of a word, and one
 //              LOP3 per code pair places code 2i in the low half and code 2i+1
