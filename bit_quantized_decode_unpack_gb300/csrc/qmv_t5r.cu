@@ -531,24 +531,33 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
             // B fragments: entry (ip, x row m, slot) at kB + ((ip M + m) 4 + slot) 16.
             // Each pass of the warp gathers from one x row (rows are 512 bytes
             // apart in the staging buffer: mixing them would stack bank conflicts)
-#pragma unroll 2
-            for (int k = 0; k < 4 * M; ++k) {
-                const int m = k >> 2, el = ((k & 3) << 5) | lane;
-                const int ip = el >> 2, slot = el & 3;
-                const int e = (ip * M + m) * 4 + slot;
-                const uint4 kw = *reinterpret_cast<const uint4 *>(&koff[(ip * 4 + slot) * 8]);
-                const uint32_t xm = xb + (uint32_t)(512 * m);
-                const uint32_t o[8] = {xm + (kw.x & 0xffffu), xm + (kw.x >> 16), xm + (kw.y & 0xffffu), xm + (kw.y >> 16),
-                                       xm + (kw.z & 0xffffu), xm + (kw.z >> 16), xm + (kw.w & 0xffffu), xm + (kw.w >> 16)};
-                uint32_t h[8];
+            // (two passes at a time: their 16 gathers are issued before either
+            // store, so that their latencies overlap)
+            for (int k = 0; k < 4 * M; k += 2) {
+                uint32_t h[2][8];
+                int e[2];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    uint16_t v16;
-                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v16) : "r"(o[q]));
-                    h[q] = v16;
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int m = (k + kk) >> 2, el = (((k + kk) & 3) << 5) | lane;
+                    const int ip = el >> 2, slot = el & 3;
+                    e[kk] = (ip * M + m) * 4 + slot;
+                    const uint4 kw = *reinterpret_cast<const uint4 *>(&koff[(ip * 4 + slot) * 8]);
+                    const uint32_t xm = xb + (uint32_t)(512 * m);
+                    const uint32_t o[8] = {xm + (kw.x & 0xffffu), xm + (kw.x >> 16), xm + (kw.y & 0xffffu),
+                                           xm + (kw.y >> 16),     xm + (kw.z & 0xffffu), xm + (kw.z >> 16),
+                                           xm + (kw.w & 0xffffu), xm + (kw.w >> 16)};
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        uint16_t v16;
+                        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v16) : "r"(o[q]));
+                        h[kk][q] = v16;
+                    }
                 }
-                sts128(st + SL::kB + (uint32_t)(e * 16), make_uint4(__byte_perm(h[0], h[1], 0x5410), __byte_perm(h[2], h[3], 0x5410),
-                                                                   __byte_perm(h[4], h[5], 0x5410), __byte_perm(h[6], h[7], 0x5410)));
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk)
+                    sts128(st + SL::kB + (uint32_t)(e[kk] * 16),
+                           make_uint4(__byte_perm(h[kk][0], h[kk][1], 0x5410), __byte_perm(h[kk][2], h[kk][3], 0x5410),
+                                      __byte_perm(h[kk][4], h[kk][5], 0x5410), __byte_perm(h[kk][6], h[kk][7], 0x5410)));
             }
             // every lane's reads of the buffer are done before any lane's copy
             // of this producer's next chunk rewrites it
@@ -556,48 +565,59 @@ __global__ void __launch_bounds__(Cta<NW>::kThreads, Cta<NW>::kPerSM)
             if (it + kProdR < ncl) issue_x(it + kProdR);
             if constexpr (COL) {
                 // Sx (row 0) and Cx (row 1) of every (period, slot, x row): the
-                // consumers' MMA sequence (two chains per period) over a constant A
+                // consumers' MMA sequence (two chains per period) over a constant A.
+                // The periods' chains are interleaved (each keeps its own order, so
+                // the sums are the consumers' bit for bit): one warp runs them, and
+                // period after period their latencies would add up
+                float d2[NG][2][4];
 #pragma unroll
-                for (int P = 0; P < NG; ++P) {
-                    float d2[2][4];
+                for (int P = 0; P < NG; ++P)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) d2[0][q] = d2[1][q] = 0.f;
+                    for (int q = 0; q < 4; ++q) d2[P][0][q] = d2[P][1][q] = 0.f;
 #pragma unroll
-                    for (int i = 0; i < MPG; i += 2) {
+                for (int i = 0; i < MPG; i += 2) {
+#pragma unroll
+                    for (int P = 0; P < NG; ++P) {
                         const int ic = P * MPG + i;
                         const uint4 bv = lds128r(st + bqo + (uint32_t)(ic >> 1) * bstride);
-                        mma_r(d2[(i >> 1) & 1], aofs[item_off<GS>(2 * i)], 0u, aofs[item_off<GS>(2 * i + 1)], 0u, bv.x, bv.y);
-                        mma_r(d2[(i >> 1) & 1], aofs[item_off<GS>(2 * i + 2)], 0u, aofs[item_off<GS>(2 * i + 3)], 0u, bv.z,
-                              bv.w);
+                        mma_r(d2[P][(i >> 1) & 1], aofs[item_off<GS>(2 * i)], 0u, aofs[item_off<GS>(2 * i + 1)], 0u, bv.x,
+                              bv.y);
+                        mma_r(d2[P][(i >> 1) & 1], aofs[item_off<GS>(2 * i + 2)], 0u, aofs[item_off<GS>(2 * i + 3)], 0u,
+                              bv.z, bv.w);
                     }
-                    if (g < 2) {
+                }
+                if (g < 2) {
+#pragma unroll
+                    for (int P = 0; P < NG; ++P) {
                         const uint32_t a = st + (uint32_t)SL::sx_off(M) + (uint32_t)((P * 4 + t) * 16 + 4 * g);
                         // float4 {Sx(x row 0), Cx(0), Sx(1), Cx(1)}: thread g writes elements g, g + 2
-                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(d2[0][0] + d2[1][0]) : "memory");
-                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(a + 8), "f"(d2[0][1] + d2[1][1]) : "memory");
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(d2[P][0][0] + d2[P][1][0]) : "memory");
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(a + 8), "f"(d2[P][0][1] + d2[P][1][1]) : "memory");
                     }
                 }
             } else {
                 // group sums on the tensor core: D[r][m] = Sx[group r][x row m];
                 // thread (g, t) holds groups g, g+8 of x rows 2t, 2t+1
                 {
-                    float d4[4][4];
+                    // eight accumulator chains, one warp: their latencies overlap
+                    float d4[8][4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) d4[q][0] = d4[q][1] = d4[q][2] = d4[q][3] = 0.f;
+                    for (int q = 0; q < 8; ++q) d4[q][0] = d4[q][1] = d4[q][2] = d4[q][3] = 0.f;
 #pragma unroll
                     for (int P = 0; P < NG; ++P)
 #pragma unroll
                         for (int i = 0; i < MPG; i += 2) {
                             const int ic = P * MPG + i;
                             const uint4 bv = lds128r(st + bqo + (uint32_t)(ic >> 1) * bstride);
-                            mma_r(d4[(ic >> 1) & 3], ind0[P], ind1[P], ind0[P], ind1[P], bv.x, bv.y);
-                            mma_r(d4[(ic >> 1) & 3], ind0[P], ind1[P], ind0[P], ind1[P], bv.z, bv.w);
+                            mma_r(d4[(ic >> 1) & 7], ind0[P], ind1[P], ind0[P], ind1[P], bv.x, bv.y);
+                            mma_r(d4[(ic >> 1) & 7], ind0[P], ind1[P], ind0[P], ind1[P], bv.z, bv.w);
                         }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int r = g + 8 * (q >> 1), m = 2 * t + (q & 1);
                         if (r < GPC && m < M) {
-                            const float v = (d4[0][q] + d4[1][q]) + (d4[2][q] + d4[3][q]);
+                            const float v =
+                                ((d4[0][q] + d4[1][q]) + (d4[2][q] + d4[3][q])) + ((d4[4][q] + d4[5][q]) + (d4[6][q] + d4[7][q]));
                             const __half hi = __float2half_rn(v);
                             const __half lo = __float2half_rn(v - __half2float(hi));
                             // bias MMA nb: slots 2t, 2t+1 <- group NG t + 2nb, slots 2t+8, 2t+9 <- group NG t + 2nb + 1
