@@ -28,8 +28,10 @@
 // CTA's rows chunk by chunk (256 codes per row) into
 // the ring: the weight tile with one 2-D TMA copy (64- or 32-byte swizzle, so
 // the quads' 32-bit reads hit 32 distinct banks), the tile's scales and
-// biases once per CTA, all completing on mbarriers.  Weights, scales and
-// biases are requested before the programmatic-dependent-launch wait.
+// biases once per CTA (one TMA box each when a row of them is a multiple of
+// 16 bytes, else 4-byte cp.async copies by every thread), all completing on
+// mbarriers.  Weights, scales and biases are requested before the
+// programmatic-dependent-launch wait.
 // K is split over the S CTAs of a thread-block cluster; the partial sums are
 // reduce-scattered through distributed shared memory (st.async completing on
 // the receiving rank's mbarrier) and added in rank order: no global scratch,
@@ -69,6 +71,7 @@ struct TmaParams {
     __half *out;
     float ratio;
     int M, N, K, G, chunks, S, Cs, stages, RS, BX;
+    int sc_tma;     // 1: scale / bias boxes by TMA; 0: by 4-byte cp.async copies (G % 8 != 0)
     uint32_t zero;  // always 0: keeps the magic constants opaque (in registers)
     unsigned long long wait_ns;  // limit of the pipeline waits
 };
@@ -85,6 +88,19 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+
+// 4 bytes global -> shared; src_bytes 0 writes zeros and reads nothing
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// one arrival on `bar` once all of this thread's earlier cp.async copies have
+// landed (counted in the barrier's expected arrivals)
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar)
 {
@@ -186,7 +202,7 @@ template <int TPW> constexpr int kRowsCT = kRowsWT<TPW> * kCons;  // weight rows
 //   weights [rows][CB] (TMA, swizzled) | B fragments [8][MP][4] uint4
 //   | Cx [4][8] f32 | Sx as fp16 (hi, lo) [8][4]
 // The scales and biases of the CTA's whole K range sit outside the ring, one
-// TMA box each: [rows][BX groups] fp16.
+// box each: [rows][BX groups] fp16, zero past row N and group G.
 // a producer's staging of one chunk of x: MP rows of 256 fp16
 template <int MP>
 constexpr int kXRawBytes = MP * kChunkT * 2;
@@ -259,7 +275,8 @@ __global__ void __launch_bounds__(kThreadsT, 2)
             mbar_init(smem_addr(&full_bar[s]), 33);
             mbar_init(smem_addr(&empty_bar[s]), kCons * 32);
         }
-        mbar_init(smem_addr(&sc_bar), 1);
+        // scale boxes: producer lane 0 (expect_tx), or every thread's copies
+        mbar_init(smem_addr(&sc_bar), p.sc_tma ? 1 : kThreadsT);
         if (S > 1) {
             // rows [rank RS, rank RS + nrow) from all S ranks, ceil(M/2) float pairs a row
             const int nrow = max(0, min(p.RS, kRowsC - rank * p.RS));
@@ -273,6 +290,20 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     // barrier set up, before any distributed-shared-memory store (the matching
     // wait is before them)
     if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    if (!p.sc_tma && ncl > 0) {
+        // rows of G fp16 that are no multiple of 16 bytes (G even, so 4-byte
+        // aligned): the boxes by 4-byte copies of two groups, every thread
+        // taking every kThreadsT-th pair; gx + j < G implies gx + j + 1 < G
+        const int hbx = p.BX >> 1;
+        for (int e = tid; e < kRowsC * hbx; e += kThreadsT) {
+            const int r = e / hbx, j = 2 * (e - r * hbx);
+            const bool in = n0 + r < p.N && gx + j < p.G;
+            const size_t off = in ? (size_t)(n0 + r) * p.G + gx + j : 0;
+            cp_async4(sc_a + (uint32_t)(4 * e), p.scales + off, in ? 4u : 0u);
+            if (HAS_BIAS) cp_async4(bi_a + (uint32_t)(4 * e), p.biases + off, in ? 4u : 0u);
+        }
+        cp_async_arrive_noinc(smem_addr(&sc_bar));
+    }
     uint32_t mg[10];
 #pragma unroll
     for (int i = 0; i < 10; ++i) mg[i] = F::magic_at(i < F::kNumMagic ? i : 0) ^ p.zero;
@@ -307,7 +338,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         const uint32_t one2 = 0x3C003C00u;
         // scales, biases and the weights of the first stages do not depend on
         // the previous kernel
-        if (pw == 0 && lane == 0 && ncl > 0) {
+        if (p.sc_tma && pw == 0 && lane == 0 && ncl > 0) {
             const uint32_t bx_bytes = (uint32_t)(kRowsC * p.BX * 2);
             mbar_arrive_expect_tx(smem_addr(&sc_bar), bx_bytes * (HAS_BIAS ? 2 : 1));
             tma_load_2d(sc_a, &smap, gx, n0, smem_addr(&sc_bar));
@@ -417,6 +448,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         // consumed before the stage was refilled), and each issued stage was
         // also prepared, so its barrier can complete: once both producers have
         // stopped issuing, each waits for the stages it filled last
+        cp_async_wait_all();
         asm volatile("bar.sync 1, %0;" ::"n"(kProd * 32) : "memory");
         if (lane == 0) {
             for (int s = 0; s < NST; ++s) {
@@ -458,6 +490,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     int s = 0;
     uint32_t par = 0;
     const bool sc_ok = ncl == 0 || wait_bounded(smem_addr(&sc_bar), 0, p.wait_ns);
+    cp_async_wait_all();  // this thread's scale copies (landed already unless the wait expired)
     for (int it = 0; it < ncl && sc_ok; ++it) {
         if (!wait_bounded(smem_addr(&full_bar[s]), par, p.wait_ns)) break;
         // scales of the four rows for the chunk's groups
@@ -722,10 +755,12 @@ int launch_t(const TmaParams &p0, const CUtensorMap &map, int chunks, cudaStream
     p.stages = pl.stages;
     p.RS = pl.RS;
     p.BX = pl.BX;
-    CUtensorMap smap, bmap;
-    if (!encode_f16(smap, p.scales, p.G, p.N, pl.BX, kRowsCT<TPW>)) return BQD_ERR_CUDA;
-    bmap = smap;
-    if (HAS_BIAS && !encode_f16(bmap, p.biases, p.G, p.N, pl.BX, kRowsCT<TPW>)) return BQD_ERR_CUDA;
+    CUtensorMap smap{}, bmap{};  // unused (zero) when the boxes are copied by cp.async
+    if (p.sc_tma) {
+        if (!encode_f16(smap, p.scales, p.G, p.N, pl.BX, kRowsCT<TPW>)) return BQD_ERR_CUDA;
+        bmap = smap;
+        if (HAS_BIAS && !encode_f16(bmap, p.biases, p.G, p.N, pl.BX, kRowsCT<TPW>)) return BQD_ERR_CUDA;
+    }
     if (opt_debug_plan())
         fprintf(stderr,
                 "bqd tma plan: N=%d K=%d M=%d gs=%d -> rows=%d S=%d Cs=%d stages=%d R=%d BX=%d grid=%dx%d smem=%zu\n",
@@ -794,12 +829,16 @@ int take_qmv_tma_timeouts(unsigned int *count)
 int launch_qmv_tma(const QmvArgs &a, cudaStream_t s)
 {
     if (a.fmt != BQD_FMT_AFFINE1 && a.fmt != BQD_FMT_AFFINE2) return BQD_ERR_UNSUPPORTED;
-    // whole 256-code chunks; the TMA boxes need 16-byte aligned bases and rows
-    // (weights: row_bytes, scales / biases: G fp16)
-    if (a.K % kChunkT != 0 || a.row_bytes % 16 != 0 || a.G % 8 != 0) return BQD_ERR_UNSUPPORTED;
+    // whole 256-code chunks; the weight tile's TMA box needs a 16-byte aligned
+    // base and rows.  Scales / biases: TMA boxes when their rows (G fp16) and
+    // bases are 16-byte aligned, else 4-byte copies (even G, 4-byte bases)
+    if (a.K % kChunkT != 0 || a.row_bytes % 16 != 0) return BQD_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(a.w) & 15) || (reinterpret_cast<uintptr_t>(a.x) & 15)) return BQD_ERR_UNSUPPORTED;
-    if ((reinterpret_cast<uintptr_t>(a.scales) & 15) || (a.biases && (reinterpret_cast<uintptr_t>(a.biases) & 15)))
-        return BQD_ERR_UNSUPPORTED;
+    auto sc_align = [&](uintptr_t m) {
+        return !(reinterpret_cast<uintptr_t>(a.scales) & m) && !(a.biases && (reinterpret_cast<uintptr_t>(a.biases) & m));
+    };
+    const bool sc_tma = a.G % 8 == 0 && sc_align(15);
+    if (!sc_tma && (a.G % 2 != 0 || !sc_align(3))) return BQD_ERR_UNSUPPORTED;
     if (a.K > (int64_t)1 << 28 || a.N > (int64_t)1 << 28) return BQD_ERR_UNSUPPORTED;
     auto enc = encode_fn();
     if (!enc) return BQD_ERR_UNSUPPORTED;
@@ -822,6 +861,7 @@ int launch_qmv_tma(const QmvArgs &a, cudaStream_t s)
     TmaParams p;
     p.scales = a.scales; p.biases = a.biases; p.ratio = a.ratio;
     p.N = (int)a.N; p.K = (int)a.K; p.G = (int)a.G;
+    p.sc_tma = sc_tma ? 1 : 0;
     p.chunks = (int)(a.K / kChunkT);
     p.zero = 0;
     p.wait_ns = (unsigned long long)opt_wait_ns();

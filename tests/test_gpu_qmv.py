@@ -76,8 +76,8 @@ def test_tensor_core_paths_forced(kernel, fmt, gs, sym):
         run_case(p, kernel)
 
 
-# TMA-ring kernel: its envelope is K a multiple of 256 with K/gs a multiple of
-# 8 (16-byte scale rows); shapes span row blocks of 128 (N <= 2048) and 256
+# TMA-ring kernel: its envelope is K a multiple of 256 (with K/gs a multiple of
+# 8 the scale rows are 16-byte multiples and come by TMA); shapes span row blocks of 128 (N <= 2048) and 256
 # (larger N) with ragged tails, both sides of N = 2048, split-K clusters of
 # many sizes (portable and not; 300 x 17408 would take 14 ranks, which leave
 # one of them no rows of a 128-row block, so the planner skips that split), M
@@ -121,11 +121,60 @@ def test_t5_tma_kernel_shapes(gs, sym):
         run_case(p, "tma")
 
 
+# K a multiple of 256 whose scale rows (K/gs fp16) are no multiple of 16 bytes:
+# the scale and bias boxes come by 4-byte copies instead of TMA.  K = 2304 at
+# gs = 128 gives 36-byte rows (4-byte aligned only); split-K clusters, passes of
+# 8 rows, 128- and 256-row blocks and ragged tails as above
+TMA_COPY_SHAPES = {64: [(1, 300, 768), (5, 1000, 1280), (3, 2100, 2304), (8, 129, 4864), (12, 257, 3840),
+                        (2, 4100, 2816), (1, 40, 768)],
+                   128: [(1, 300, 1280), (5, 1000, 2304), (3, 2100, 2560), (8, 129, 1536), (12, 257, 3584),
+                         (2, 4100, 2304), (1, 5120, 13824), (4, 64, 256)]}
+
+
+@pytest.mark.parametrize("fmt", [F1, F2])
+@pytest.mark.parametrize("gs", [64, 128])
+@pytest.mark.parametrize("sym", [False, True])
+def test_tma_kernel_scale_rows_by_copies(fmt, gs, sym):
+    for M, N, K in TMA_COPY_SHAPES[gs]:
+        assert (K // gs) % 8 != 0 and K % 256 == 0
+        run_case(synth.problem(fmt, M, N, K, gs, sym=sym), "tma")
+
+
+@pytest.mark.parametrize("fmt", [F1, F2])
+@pytest.mark.parametrize("sym", [False, True])
+def test_tma_kernel_scales_at_4_byte_offsets(fmt, sym):
+    """Scale (and bias) tensors whose storage starts 4 bytes past a 16-byte
+    boundary: the boxes come by copies although their rows are 16-byte
+    multiples."""
+    import torch
+    gs = 64
+    for M, N, K in [(3, 300, 2048), (5, 4100, 5120), (1, 129, 17408)]:
+        p = synth.problem(fmt, M, N, K, gs, sym=sym)
+        packed = oracle.c_pack(p["codes"], fmt, gs)
+        w = bqd.pack(to_dev(p["codes"]), fmt, gs)
+
+        def offset_copy(a):
+            if a is None:
+                return None
+            buf = torch.empty(a.size + 2, dtype=torch.float16, device="cuda")
+            t = buf[2:].view(a.shape)
+            t.copy_(torch.from_numpy(a))
+            assert t.data_ptr() % 16 == 4 and t.is_contiguous()
+            return t
+
+        with forced_kernel("tma"):
+            y = bqd.qmv(to_dev(p["x"]), w, offset_copy(p["scales"]), offset_copy(p["biases"]), fmt, gs)
+        torch.cuda.synchronize()
+        yr, bound = oracle.c_qmv_rows(p["x"], packed, p["scales"], p["biases"], fmt, gs)
+        assert_within_tolerance(y.cpu().numpy().astype(np.float64), yr, bound, what=p["key"])
+
+
 @pytest.mark.parametrize("fmt", [F1, F2])
 def test_tma_envelope_and_fallback(fmt):
-    """Outside the TMA kernel's envelope (here K/gs = 12 groups) a forced call
-    reports "unsupported" and the default dispatch still gives parity."""
-    p = synth.problem(fmt, 3, 100, 768, 64)
+    """Outside the TMA kernel's envelope (here K = 640, no whole number of
+    256-code chunks) a forced call reports "unsupported" and the default
+    dispatch still gives parity."""
+    p = synth.problem(fmt, 3, 100, 640, 64)
     with pytest.raises(bqd.BqdError) as ei:
         run_case(p, "tma")
     assert ei.value.status == 2  # BQD_ERR_UNSUPPORTED

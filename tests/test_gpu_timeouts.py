@@ -21,6 +21,7 @@ CASES = [
     # (kernel family, fmt, M, N, K, gs, sym): the 1/2-bit and t5 TMA-ring decode
     # kernels with split-K clusters, and the tcgen05 prefill product
     ("tma", F2, 3, 4096, 5120, 64, False),
+    ("tma", F2, 5, 2100, 2560, 128, False),  # scale boxes by 4-byte copies (20 groups a row)
     ("tma", T5, 2, 2048, 5120, 64, True),
     ("qmm", T5, 64, 1024, 2048, 128, True),
     ("qmm", F2, 64, 1024, 2048, 64, False),
