@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         // consumed before the stage was refilled), and each issued stage was
         // also prepared, so its barrier can complete: once both producers have
         // stopped issuing, each waits for the stages it filled last
-        cp_async_wait_all();
+        if (!p.sc_tma) cp_async_wait_all();  // this thread's scale copies
         asm volatile("bar.sync 1, %0;" ::"n"(kProd * 32) : "memory");
         if (lane == 0) {
             for (int s = 0; s < NST; ++s) {
@@ -490,7 +490,9 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     int s = 0;
     uint32_t par = 0;
     const bool sc_ok = ncl == 0 || wait_bounded(smem_addr(&sc_bar), 0, p.wait_ns);
-    cp_async_wait_all();  // this thread's scale copies (landed already unless the wait expired)
+    // the box barrier completes only once every thread's scale copies have
+    // landed; after an expired wait this thread's own may still be in flight
+    if (!sc_ok) cp_async_wait_all();
     for (int it = 0; it < ncl && sc_ok; ++it) {
         if (!wait_bounded(smem_addr(&full_bar[s]), par, p.wait_ns)) break;
         // scales of the four rows for the chunk's groups
