@@ -581,9 +581,11 @@ def kernel_traffic_from_profiles():
         return None
 
 
-def run_case(spec: str, sets: int, reps: int = 64):
+def run_case(spec: str, sets: int, reps: int = 64, graph: bool = False):
     """--case fmt,M,N,K,gs[,sym]: one configuration over rotating weight sets
-    (the command line used for single-kernel ncu captures)."""
+    (the command line used for single-kernel ncu captures).  With --graph the
+    reps calls also run as one CUDA graph (best of 5 replays), which takes the
+    host's launch time out of the per-call figure."""
     import torch
     import bit_quantized_decode_unpack_gb300 as bqd
     from bit_quantized_decode_unpack_gb300 import _build, synth
@@ -614,8 +616,27 @@ def run_case(spec: str, sets: int, reps: int = 64):
     e1.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / reps
     nb = call_bytes(fmt, sym or fmt == T5, M, N, K, gs)
-    print(json.dumps({"case": spec, "us_per_call_eager": us, "gbs": nb / (us * 1e-6) / 1e9,
-                      "tflops": 2.0 * M * N * K / (us * 1e-6) / 1e12}), flush=True)
+    res = {"case": spec, "us_per_call_eager": us, "gbs": nb / (us * 1e-6) / 1e9,
+           "tflops": 2.0 * M * N * K / (us * 1e-6) / 1e12}
+    if graph:
+        st = torch.cuda.Stream()
+        st.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            for i in range(reps):
+                w, s_, b_ = W[i % sets]
+                bqd.qmv(x, w, s_, b_, fmt, gs, out=y)
+        best = float("inf")
+        with torch.cuda.stream(st):
+            for r in range(8):
+                e0.record(st)
+                g.replay()
+                e1.record(st)
+                e1.synchronize()
+                if r >= 3:
+                    best = min(best, e0.elapsed_time(e1) * 1e3 / reps)
+        res.update({"us_per_call_graph": best, "gbs_graph": nb / (best * 1e-6) / 1e9})
+    print(json.dumps(res), flush=True)
     return 0
 
 
@@ -781,6 +802,7 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=120.0,
                     help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--case", type=str, default=None, help="fmt,M,N,K,gs[,sym]: time one configuration")
+    ap.add_argument("--graph", action="store_true", help="--case: also time the calls replayed from a CUDA graph")
     ap.add_argument("--group", type=str, default=None,
                     help="M,proj: the eight calls of one sweep group on their own tensors (L2 check)")
     ap.add_argument("--spec-case", type=str, default=None,
@@ -788,7 +810,7 @@ def main():
     args = ap.parse_args()
 
     if args.case:
-        return run_case(args.case, args.sets)
+        return run_case(args.case, args.sets, graph=args.graph)
     if args.group:
         return run_group(args.group)
     if args.spec_case:
